@@ -1,0 +1,528 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 dense GEMM / GEMV / expert-ID matmul hot path.
+
+One step = one pass over the whole hot path, the five synthetic workloads
+(seed 0) each called once through the C ABI, in this order so that every
+call starts with its inputs evicted from L2 by the calls before it:
+  C5  matmul_id GroupedPrefill  m=4096 E=128 top_k=8 (Zipf 1.1) k=4096 n=1536 bf16 W
+  C2  decode GEMV f16           1 x 11008 x 4096 (W stored [n,k])
+  C3  batched GEMM f16          4 x 4096 x 4096 x 4096 (B stored [n,k])
+  C4  matmul_id Direct          m=4 E=64 top_k=8 k=2048 n=1408 bf16 W
+  C1  f32 GEMM                  64 x 64 x 128
+Metric: "% of GB300 roofline" = sum over the calls of their roofline time
+(max(algorithmic flops / tensor or FFMA peak, algorithmic bytes / HBM
+peak), peaks from MEASURED_PEAKS.json) divided by the measured step time.
+With N GPUs (torchrun) every rank runs the same step (replicas: the path has
+no exchange step); value = N * sum(roofline) / max-over-ranks step time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--only c1,c2,...] [--no-e2e] [--no-cpu-baseline]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemv_moe_expert_gb300 import synth  # noqa: E402
+
+ORDER = ["c5", "c2", "c3", "c4", "c1"]
+NAMES = {"c1": "c1_f32_gemm", "c2": "c2_f16_gemv", "c3": "c3_f16_gemm",
+         "c4": "c4_moe_direct", "c5": "c5_moe_grouped"}
+METRIC = "GEMM TFLOP/s and GEMV/matmul_id GB/s, as % of GB300 roofline"
+UNIT = "% of GB300 roofline (sum of per-call roofline times / step time)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ffma_peak_tflops(sm_mhz: float = 2070.0, sms: int = 152) -> float:
+    # 128 FP32 FMA lanes per SM per clock, 2 flops per FMA
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ---------------------------------------------------------------------------
+# per-workload algorithmic work
+# ---------------------------------------------------------------------------
+
+def work_of(key: str, w) -> dict:
+    if key in ("c1", "c2", "c3"):
+        size = synth.ITEMSIZE[w.dtype]
+        flops = 2 * w.batch * w.m * w.n * w.k
+        bytes_ = (w.a.size + w.b.size + w.batch * w.m * w.n) * size
+        bound = "tensor" if key == "c3" else ("hbm" if key == "c2" else "ffma")
+        return {"flops": flops, "bytes": bytes_, "bound": bound}
+    c = w
+    wsize = synth.ITEMSIZE[c.wdtype]
+    expert_bytes = c.n * c.k * wsize
+    distinct = len(np.unique(c.ids.reshape(-1)[c.ids.reshape(-1) < c.n_experts]))
+    flops = 2 * c.m * c.top_k * c.n * c.k
+    if key == "c4":
+        # the distinct experts of the call are read once
+        bytes_ = distinct * expert_bytes + c.x.nbytes + c.ids.nbytes + c.m * c.top_k * c.n * 4
+        return {"flops": flops, "bytes": bytes_, "bound": "hbm", "distinct_experts": distinct}
+    bytes_ = c.n_experts * expert_bytes + c.x.nbytes + c.ids.nbytes + c.m * c.top_k * c.n * 4
+    return {"flops": flops, "bytes": bytes_, "bound": "hbm+tensor", "distinct_experts": distinct}
+
+
+def roofline_seconds(wk: dict, peaks: dict, tensor_peak_tf: float) -> float:
+    t_bytes = wk["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if wk["bound"] == "ffma":
+        t_flops = wk["flops"] / (ffma_peak_tflops() * 1e12)
+    else:
+        t_flops = wk["flops"] / (tensor_peak_tf * 1e12)
+    return max(t_bytes, t_flops)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (the oracle as it stands, on a bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_seconds(key: str, w, outputs: int, threads: int) -> tuple[float, int, int]:
+    """Time the oracle on `outputs` sampled elements; returns (seconds,
+    sampled outputs, total outputs)."""
+    import oracle
+    rng = np.random.default_rng(123)
+    if key in ("c1", "c2", "c3"):
+        total = w.batch * w.m * w.n
+        cnt = min(outputs, total)
+        idx = rng.choice(total, cnt, replace=False).astype(np.int64) if cnt < total else None
+        t0 = time.perf_counter()
+        oracle.gemm(w.dtype, w.batch, w.m, w.n, w.k, w.ta, w.tb, w.a.reshape(-1), w.lda,
+                    w.stride_a, w.b.reshape(-1), w.ldb, w.stride_b, idx=idx, nthreads=threads)
+        return time.perf_counter() - t0, cnt, total
+    c = w
+    total = c.m * c.top_k * c.n
+    cnt = min(outputs, total)
+    idx = rng.choice(total, cnt, replace=False).astype(np.int64) if cnt < total else None
+    t0 = time.perf_counter()
+    oracle.matmul_id(c.wdtype, c.m, c.n, c.k, c.top_k, c.n_experts, c.expert_stride_bytes,
+                     c.input_layout, c.w, c.x, c.ids, idx=idx, nthreads=threads)
+    if key == "c5":
+        oracle.map_distinct(c.m, c.top_k, c.n_experts, c.ids)
+    return time.perf_counter() - t0, cnt, total
+
+
+SAMPLE_OUTPUTS = {"c1": 4096, "c2": 11008, "c3": 32768, "c4": 45056, "c5": 32768}
+
+
+def cpu_baseline(workloads: dict, roof_total: float, scale: float = 1.0) -> dict:
+    cb = cpu_baseline_keys(workloads, [k for k in ORDER if k in workloads], roof_total, scale)
+    est_total = cb["est_step_seconds"]
+    return {"value": 100.0 * roof_total / est_total, "unit": UNIT, "cores": cb["cores"],
+            "kind": "oracle",
+            "sample": cb["sample"] + f"; full-step time extrapolated by outputs: "
+                                     f"{est_total:.1f} s per step",
+            "est_step_seconds": est_total}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+class Problem:
+    """Device buffers and the call of one workload."""
+
+    def __init__(self, key, w, torch, gb):
+        self.key, self.w = key, w
+        self.torch, self.gb = torch, gb
+        dev = torch.device("cuda")
+
+        def up(arr):
+            return torch.from_numpy(np.ascontiguousarray(arr).reshape(-1).view(np.uint8).copy()).to(dev)
+
+        self.host_inputs = []
+        if key in ("c1", "c2", "c3"):
+            self.a, self.b = up(w.a), up(w.b)
+            self.c = torch.empty(w.batch * w.m * w.n * synth.ITEMSIZE[w.dtype], dtype=torch.uint8,
+                                 device=dev)
+            self.host_inputs = [w.a, w.b]
+            self.outputs = [self.c]
+            self.launches = 1
+        else:
+            c = w
+            self.wt, self.x, self.ids = up(c.w), up(c.x), up(c.ids)
+            self.params = gb.make_params(c.m, c.n, c.k, c.top_k, c.n_experts, c.expert_stride_bytes,
+                                         c.input_layout, c.multiplicity, c.route)
+            st, cap = gb.gbmm_matmul_id_capability(c.wdtype, self.params)
+            gb.check(st)
+            self.cap = cap
+            self.out = torch.empty(cap.required_output_bytes, dtype=torch.uint8, device=dev)
+            self.scratch = None
+            if c.route == 1:
+                self.counts = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device=dev)
+                self.rows = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device=dev)
+                self.scratch = gb.make_scratch(self.counts, cap.expert_counts_bytes, self.rows,
+                                               cap.routed_rows_bytes, c.n_experts, c.m)
+            self.host_inputs = [c.w, c.x, c.ids]
+            self.outputs = [self.out]
+            self.launches = 2 if c.route == 1 else 1
+
+    def device_inputs(self):
+        if self.key in ("c1", "c2", "c3"):
+            return [self.a, self.b]
+        return [self.wt, self.x, self.ids]
+
+    def call(self, stream):
+        gb, w = self.gb, self.w
+        if self.key in ("c1", "c2", "c3"):
+            fn = gb.gbmm_gemv if self.key == "c2" else gb.gbmm_gemm
+            st = fn(w.dtype, w.batch, w.m, w.n, w.k, w.ta, w.tb, self.a, 0, w.lda, w.stride_a,
+                    self.b, 0, w.ldb, w.stride_b, self.c, 0, w.ldc, w.stride_c, stream)
+        else:
+            c = w
+            st, _ = gb.gbmm_matmul_id(self.params, c.wdtype, self.wt, c.w.nbytes, self.x,
+                                      c.x.nbytes, self.ids, c.ids.nbytes, self.out,
+                                      self.cap.required_output_bytes, self.scratch, stream)
+        if st != gb.GBMM_OK:
+            raise RuntimeError(f"{self.key}: {gb.gbmm_status_string(st)}: {gb.gbmm_last_error()}")
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args) -> None:
+    import torch
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from gemv_moe_expert_gb300 import binding as gb
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+
+    keys = [k for k in ORDER if k in args.only]
+    peaks, peak_src = load_peaks()
+    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    workloads = {k: synth.workload(NAMES[k]) for k in keys}
+    works = {k: work_of(k, workloads[k]) for k in keys}
+    roof = {k: roofline_seconds(works[k], peaks, tensor_peak) for k in keys}
+    roof_total = sum(roof.values())
+
+    probs = {k: Problem(k, workloads[k], torch, gb) for k in keys}
+    stream = torch.cuda.Stream()
+    sptr = int(stream.cuda_stream)
+    n_launch = sum(p.launches for p in probs.values())
+
+    def step(events=None):
+        for i, k in enumerate(keys):
+            if events is not None:
+                events[i].record(stream)
+            probs[k].call(sptr)
+        if events is not None:
+            events[len(keys)].record(stream)
+
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # per-call durations from events between the launches of each step
+    per_call = {k: 0.0 for k in keys}
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(keys) + 1)]
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    gb.gbmm_test_reset_launch_count()
+    t_wall = time.perf_counter()
+    start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    launches = gb.gbmm_test_launch_count()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.1)
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    for s in range(args.steps):
+        for i, k in enumerate(keys):
+            per_call[k] += ev[s][i].elapsed_time(ev[s][i + 1])
+    per_call = {k: v / args.steps for k, v in per_call.items()}
+
+    t_local = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(t_local.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = 100.0 * world * roof_total / (ms_per_step / 1e3)
+
+    # ---- end to end: pinned host inputs in, results out, every step ----
+    e2e = None
+    if not args.no_e2e:
+        pinned_in, pinned_out = [], []
+        pairs_in, pairs_out = [], []
+        for k in keys:
+            p = probs[k]
+            for host, dev_t in zip(p.host_inputs, p.device_inputs()):
+                h = torch.from_numpy(np.ascontiguousarray(host).reshape(-1).view(np.uint8).copy())
+                h = h.pin_memory()
+                pinned_in.append(h)
+                pairs_in.append((dev_t, h))
+            for dev_t in p.outputs:
+                h = torch.empty(dev_t.numel(), dtype=torch.uint8).pin_memory()
+                pinned_out.append(h)
+                pairs_out.append((h, dev_t))
+        h2d = sum(h.numel() for h in pinned_in)
+        d2h = sum(h.numel() for h in pinned_out)
+        e2e_steps = max(1, min(args.steps, 5))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for dev_t, h in pairs_in:
+                    dev_t.copy_(h, non_blocking=True)
+                step()
+                for h, dev_t in pairs_out:
+                    h.copy_(dev_t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1) / e2e_steps
+        t_e = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(t_e, op=dist.ReduceOp.MAX)
+        e_ms = float(t_e.item())
+        e2e = {"value": 100.0 * world * roof_total / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms, "steps": e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # per-call report and the dominant kernel's roofline
+    calls = {}
+    for k in keys:
+        wk = works[k]
+        secs = per_call[k] / 1e3
+        entry = {"ms": per_call[k], "roofline_ms": roof[k] * 1e3,
+                 "frac_of_roofline": roof[k] / secs if secs > 0 else None,
+                 "achieved_gbs": wk["bytes"] / secs / 1e9 if secs > 0 else None,
+                 "achieved_tflops": wk["flops"] / secs / 1e12 if secs > 0 else None,
+                 "algorithmic_bytes": wk["bytes"], "algorithmic_flops": wk["flops"]}
+        if "distinct_experts" in wk:
+            entry["distinct_experts"] = wk["distinct_experts"]
+        calls[k] = entry
+    dom = max(keys, key=lambda k: per_call[k])
+    wk = works[dom]
+    secs = per_call[dom] / 1e3
+    if wk["bound"] in ("tensor",):
+        achieved = wk["flops"] / secs / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak,
+                    "unit": "TFLOP/s", "frac": achieved / tensor_peak}
+    else:
+        achieved = wk["bytes"] / secs / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}
+    roofline.update({"kernel": dom, "peak_source": peak_src,
+                     "peak_kind": "sustained" if roofline["bound"] == "tensor" else "copy",
+                     "traffic": TRAFFIC.get(dom)})
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(workloads, roof_total, args.cpu_scale)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16/bf16 in, f32 accumulate (f32 for c1)",
+        "data": "synthetic (seeded numpy, seed 0)",
+        "config": {"workload": "hot path: " + " + ".join(NAMES[k] for k in keys),
+                   "calls_per_step": len(keys), "launches_per_step": n_launch,
+                   "l2": "inputs larger than L2 between calls: c5 streams 1.88 GB, each call's "
+                         "inputs evicted by the calls before it",
+                   "parallelism": f"replicas x{world}", "peaks": {k: peaks[k] for k in
+                                                                   ("hbm_gbs", "bf16_tflops",
+                                                                    "bf16_tflops_sustained")
+                                                                   if k in peaks},
+                   "roofline_ms_per_step": roof_total * 1e3, "calls": calls},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+        "clocks": clk, "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# DRAM traffic per launch from ncu (bytes), by workload; None until captured
+# for the current kernel.
+TRAFFIC: dict = {}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle, as it stands, on the machine's host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args) -> None:
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    keys = [k for k in ORDER if k in args.only]
+    peaks, _ = load_peaks()
+    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    workloads = {k: synth.workload(NAMES[k]) for k in keys}
+    roof_total = sum(roofline_seconds(work_of(k, workloads[k]), peaks, tensor_peak) for k in keys)
+    scale = args.cpu_scale * 0.25
+    for _ in range(args.warmup):
+        cpu_baseline_keys(workloads, keys, roof_total, scale * 0.05)
+    ests = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cb = cpu_baseline_keys(workloads, keys, roof_total, scale)
+        ests.append(cb["est_step_seconds"])
+    wall = time.perf_counter() - t0
+    est = statistics.mean(ests)
+    value = 100.0 * roof_total / est
+    cpu = {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+           "sample": cb["sample"]}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (oracle)",
+            "data": "synthetic (seeded numpy, seed 0)", "impl": "reference",
+            "config": {"workload": "hot path: " + " + ".join(NAMES[k] for k in keys),
+                       "note": "the CPU oracle timed on sampled outputs of each call and "
+                               "extrapolated to the full step"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s_timed": wall}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_keys(workloads, keys, roof_total, scale):
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    est_total, parts = 0.0, []
+    for key in keys:
+        n_out = max(1, int(SAMPLE_OUTPUTS[key] * scale))
+        secs, cnt, total = oracle_sample_seconds(key, workloads[key], n_out, threads)
+        est_total += secs * total / cnt
+        parts.append(f"{key}:{cnt}/{total}")
+    return {"cores": threads, "est_step_seconds": est_total,
+            "sample": "sampled outputs per call (" + ", ".join(parts) + ")"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", default=",".join(ORDER))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-scale", type=float, default=1.0)
+    args = ap.parse_args()
+    args.only = [k.strip() for k in args.only.split(",") if k.strip()]
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

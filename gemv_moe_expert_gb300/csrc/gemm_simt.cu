@@ -1,0 +1,124 @@
+// gemm_simt.cu -- general strided GEMM on the FFMA pipe (f32 accumulation),
+// any transposes, leading dims, batch strides and tails.  It serves the f32
+// GEMM and every f16/bf16 layout the tensor-core path does not take.
+//
+// Semantics: tract-metal 0.23.6, src/kernels/matmul/mlx_gemm/mod.rs,
+// `dispatch_metal_mlx_gemm` (A stored [k, m] when transposed, B stored
+// [n, k] when transposed), and rlx-metal 0.2.14, src/mps_blas.rs,
+// `encode_mps_sgemm_t`.
+//
+// CTA tile 64 x 64 x 16, 256 threads, 4 x 4 outputs per thread; operands are
+// staged through shared memory as f32 with the global loads ordered along the
+// contiguous dimension of each operand (coalesced for every transpose flag).
+#include "device_common.cuh"
+
+namespace gbmm {
+
+namespace {
+
+constexpr int kBM = 64;
+constexpr int kBN = 64;
+constexpr int kBK = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmParams p) {
+    __shared__ float As[kBK][kBM + 4];
+    __shared__ float Bs[kBK][kBN + 4];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kBM;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBN;
+
+    for (int64_t bat = blockIdx.z; bat < p.batch; bat += gridDim.z) {
+        const T *A = static_cast<const T *>(p.a) + bat * p.sa;
+        const T *B = static_cast<const T *>(p.b) + bat * p.sb;
+        T *C = static_cast<T *>(p.c) + bat * p.sc;
+        float acc[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+
+        for (int64_t k0 = 0; k0 < p.k; k0 += kBK) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int idx = tid + e * 256;
+                int i, x;
+                if (p.ta) {  // A stored [k][m]: walk i fastest
+                    i = idx % kBM;
+                    x = idx / kBM;
+                } else {     // A stored [m][k]: walk x fastest
+                    x = idx % kBK;
+                    i = idx / kBK;
+                }
+                const int64_t gi = m0 + i, gx = k0 + x;
+                float v = 0.f;
+                if (gi < p.m && gx < p.k)
+                    v = Elem<T>::to_f(A[p.ta ? gx * p.lda + gi : gi * p.lda + gx]);
+                As[x][i] = v;
+
+                int j, y;
+                if (p.tb) {  // B stored [n][k]: walk x fastest
+                    y = idx % kBK;
+                    j = idx / kBK;
+                } else {     // B stored [k][n]: walk j fastest
+                    j = idx % kBN;
+                    y = idx / kBN;
+                }
+                const int64_t gj = n0 + j, gy = k0 + y;
+                float w = 0.f;
+                if (gj < p.n && gy < p.k)
+                    w = Elem<T>::to_f(B[p.tb ? gj * p.ldb + gy : gy * p.ldb + gj]);
+                Bs[y][j] = w;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int x = 0; x < kBK; ++x) {
+                float av[4], bv[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) av[r] = As[x][ty + 16 * r];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) bv[c] = Bs[x][tx + 16 * c];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int64_t gi = m0 + ty + 16 * r;
+            if (gi >= p.m) continue;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int64_t gj = n0 + tx + 16 * c;
+                if (gj < p.n) C[gi * p.ldc + gj] = Elem<T>::from_f(acc[r][c]);
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t simt_t(const GemmParams &p, cudaStream_t s) {
+    const int64_t gx = (p.n + kBN - 1) / kBN;
+    const int64_t gy = (p.m + kBM - 1) / kBM;
+    if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
+    const unsigned gz = static_cast<unsigned>(p.batch < 65535 ? p.batch : 65535);
+    gemm_simt_kernel<T><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), gz), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s) {
+    switch (dt) {
+    case kF32: return simt_t<float>(p, s);
+    case kF16: return simt_t<__half>(p, s);
+    case kBF16: return simt_t<__nv_bfloat16>(p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbmm

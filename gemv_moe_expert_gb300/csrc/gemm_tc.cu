@@ -1,0 +1,305 @@
+// gemm_tc.cu -- batched f16/bf16 GEMM on the sm_103a tensor cores:
+// C[b] = A[b] * B[b]^T with A [m, k] and B [n, k] both K-contiguous (the
+// transpose_b layout), f32 accumulation in tensor memory, f16/bf16 output.
+//
+// Semantics: tract-metal 0.23.6, src/kernels/matmul/mlx_gemm/mod.rs,
+// `dispatch_metal_mlx_gemm` (B stored [n, k] when transposed; batch strides
+// per operand) and rlx-metal 0.2.14, src/mps_blas.rs (transposeRight).
+//
+// Design (one persistent CTA per SM, 6 warps, warp-specialised):
+//   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles, 128-byte
+//               swizzled, into a 4-stage shared-memory ring (48 KB/stage).
+//   warp 1      allocates 512 TMEM columns (two 128x256 f32 accumulators)
+//               and issues tcgen05.mma (M=128, N=256, K=16) from one thread;
+//               tcgen05.commit releases a stage when its MMAs are done and
+//               signals the epilogue when a tile's accumulator is complete.
+//   warps 2..5  epilogue: tcgen05.ld of their TMEM lane quarter, round to the
+//               output dtype, store; then hand the accumulator back, so the
+//               next tile's MMAs overlap this tile's stores.
+// Tiles are visited in a grouped raster (8 m-blocks x all n-blocks per group)
+// so the CTAs running at the same time share A and B panels in L2.
+// Every mbarrier wait is bounded; on a timeout the kernel records it in the
+// device error word, waits (bounded) for its own copies and MMAs in flight,
+// releases its TMEM and returns.
+#include "device_common.cuh"
+
+namespace gbmm {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;  // 64 x 2 bytes = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kGroupM = 8;
+constexpr uint32_t kABytes = kBM * kBK * 2;
+constexpr uint32_t kBBytes = kBN * kBK * 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSmemBytes = kStages * (kABytes + kBBytes) + 256 + 1024;
+
+struct TileCoord {
+    int bat, mb, nb;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int tile, const GemmTcParams &p) {
+    const int per_batch = p.tiles_m * p.tiles_n;
+    TileCoord t;
+    t.bat = tile / per_batch;
+    const int r = tile % per_batch;
+    const int group = r / (kGroupM * p.tiles_n);
+    const int first_m = group * kGroupM;
+    const int gm = min(kGroupM, p.tiles_m - first_m);
+    const int local = r % (kGroupM * p.tiles_n);
+    t.mb = first_m + local % gm;
+    t.nb = local / gm;
+    return t;
+}
+
+template <typename TC>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <typename TC, uint32_t kFmt>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const GemmTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t s_a = raw_addr + pad;
+    const uint32_t s_b = s_a + kStages * kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * (kABytes + kBBytes));
+    // barrier slots: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kblocks = (p.k + kBK - 1) / kBK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+                const TileCoord tc = decode_tile(tile, p);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), kABytes + kBBytes);
+                    tma_load_3d(s_a + stage * kABytes, &map_a, full_bar(stage), kb * kBK, tc.mb * kBM,
+                                p.a_bcast ? 0 : tc.bat);
+                    tma_load_3d(s_b + stage * kBBytes, &map_b, full_bar(stage), kb * kBK, tc.nb * kBN,
+                                p.b_bcast ? 0 : tc.bat);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report_device_error(p.err, kKidGemmTc);
+                // wait for this CTA's own copies still in flight
+                for (int s = 0; s < kStages; ++s) {
+                    const uint32_t n_s = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
+                    if (n_s > 0) mbar_wait_bounded(full_bar(s), (n_s - 1u) & 1u, p.wait_limit_ns, nullptr);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t kIdesc = idesc_f16(kFmt, kBM, kBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t da = sdesc_kmajor_sw128(s_a + stage * kABytes + kk * 32);
+                        const uint64_t db = sdesc_kmajor_sw128(s_b + stage * kBBytes + kk * 32);
+                        umma_f16_ss(d_tmem, da, db, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report_device_error(p.err, kKidGemmTc);
+            }
+            // every MMA this thread issued has completed once this arrives
+            umma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, nullptr);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            const TileCoord tc = decode_tile(tile, p);
+            // one lane waits and the warp follows its verdict, so the warp stays
+            // converged for the .sync.aligned TMEM loads below
+            int ready = 0;
+            if (lane == 0) ready = mbar_wait_bounded(tfull_bar(acc), acc_phase, p.wait_limit_ns, abort_flag);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    report_device_error(p.err, kKidGemmTc);
+                }
+                break;
+            }
+            __syncwarp();
+            tc_fence_after();
+            const int64_t row = static_cast<int64_t>(tc.mb) * kBM + quarter * 32 + lane;
+            TC *crow = static_cast<TC *>(p.c) + static_cast<int64_t>(tc.bat) * p.sc + row * p.ldc;
+            const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                    static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+            for (int chunk = 0; chunk < kBN / 32; ++chunk) {
+                uint32_t r[32];
+                tmem_ld32(t_addr + chunk * 32, r);
+                tmem_ld_wait();
+                const int64_t col0 = static_cast<int64_t>(tc.nb) * kBN + chunk * 32;
+                if (row < p.m && col0 < p.n) {
+                    if (p.c_vec_ok && col0 + 32 <= p.n) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack2<TC>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                            o.y = pack2<TC>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                            o.z = pack2<TC>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                            o.w = pack2<TC>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            dst[v] = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (col0 + c < p.n) crow[col0 + c] = Elem<TC>::from_f(__uint_as_float(r[c]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <typename TC, uint32_t kFmt>
+cudaError_t tc_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
+                 cudaStream_t s) {
+    static unsigned long long attr_set = 0;  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<TC, kFmt>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set |= bit;
+    }
+    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    gemm_tc_kernel<TC, kFmt><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tc_block_m() { return kBM; }
+int gemm_tc_block_n() { return kBN; }
+int gemm_tc_block_k() { return kBK; }
+
+cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                           const GemmTcParams &p, int num_sms, cudaStream_t s) {
+    switch (dt) {
+    case kF16: return tc_t<__half, 0>(map_a, map_b, p, num_sms, s);
+    case kBF16: return tc_t<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbmm

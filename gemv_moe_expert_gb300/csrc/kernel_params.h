@@ -1,0 +1,111 @@
+// kernel_params.h -- parameter blocks passed by value from the host dispatch
+// (api.cu) to the kernels, and the internal launcher declarations.  Plain C++
+// structs: no torch types anywhere in the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbmm {
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+inline int dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
+
+// device error word bits
+constexpr uint32_t kErrWaitTimeout = 1u;
+
+// kernel ids reported in bits 8..15 of the device error word
+enum KernelId : uint32_t {
+    kKidNone = 0,
+    kKidGemmTc = 1,
+    kKidGroupedTc = 2,
+    kKidBoundedWaitTest = 3,
+};
+
+// default limit of a bounded device wait (1 s)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Matrix-times-vector problem after the host has mapped (batch, m, n, k,
+// transposes, strides) onto "rows" outputs, each a dot product of length k.
+// All strides in elements.
+//   mat(o, x) = mat[bat*mat_bs + o*mat_rs + x*mat_ks]
+//   vec_r(x)  = vec[bat*vec_bs + r*vec_rr + x*vec_ks]     (r < nvec)
+//   out_r(o)  = out[bat*out_bs + r*out_rr + o*out_os]
+struct GemvParams {
+    const void *mat;
+    const void *vec;
+    void *out;
+    int64_t rows, k, batch;
+    int64_t mat_rs, mat_ks, mat_bs;
+    int64_t vec_ks, vec_rr, vec_bs;
+    int64_t out_os, out_rr, out_bs;
+    int32_t nvec;     // vectors sharing one pass over the matrix (1..16)
+    int32_t vec_ok;   // 16-byte vector path legal (host-checked alignment)
+};
+
+// General strided GEMM (FFMA pipe).  Same addressing as the public API.
+struct GemmParams {
+    const void *a;
+    const void *b;
+    void *c;
+    int64_t batch, m, n, k;
+    int64_t lda, ldb, ldc;
+    int64_t sa, sb, sc;
+    int32_t ta, tb;
+};
+
+// Tensor-core GEMM: A [batch][m][k] and B [batch][n][k], K-contiguous, read by
+// TMA through the two tensor maps; C written with ldc / sc.
+struct GemmTcParams {
+    void *c;
+    int64_t ldc, sc;
+    int32_t m, n, k, batch;
+    int32_t a_bcast, b_bcast;   // batch stride 0: always batch coordinate 0
+    int32_t c_vec_ok;           // C rows allow 16-byte stores
+    int32_t tiles_m, tiles_n;
+    int32_t num_tiles;
+    uint32_t *err;
+    uint64_t wait_limit_ns;
+};
+
+// Expert-ID matmul (all routes).
+struct MatmulIdParams {
+    const void *w;
+    const float *x;
+    const uint32_t *ids;
+    float *out;
+    uint32_t *counts;        // grouped route scratch
+    uint32_t *routed_rows;   // grouped route scratch, row stride m
+    int64_t m, n, k, top_k, n_experts;
+    int64_t expert_stride_elems;
+    int64_t x_token_stride, x_slot_stride;   // elements
+    int64_t total_rows;                      // m * top_k
+    uint32_t *err;
+    uint64_t wait_limit_ns;
+};
+
+// ---- launchers (each returns the launch's cudaError_t) --------------------
+
+cudaError_t launch_fill_zero(int dt, void *c, int64_t batch, int64_t m, int64_t n, int64_t ldc,
+                             int64_t sc, cudaStream_t s);
+cudaError_t launch_gemv_rowdot(int dt, const GemvParams &p, cudaStream_t s);
+cudaError_t launch_gemv_coldot(int dt, const GemvParams &p, cudaStream_t s);
+cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s);
+cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                           const GemmTcParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream_t s);
+cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s);
+cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s);
+cudaError_t launch_bounded_wait_test(uint32_t *err, uint64_t limit_ns, cudaStream_t s);
+
+int gemm_tc_block_m();
+int gemm_tc_block_n();
+int gemm_tc_block_k();
+int device_sm_count();
+
+// device address of the error word on the current device (nullptr on failure)
+uint32_t *device_error_word();
+
+}  // namespace gbmm

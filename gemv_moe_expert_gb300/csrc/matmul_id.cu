@@ -1,0 +1,421 @@
+// matmul_id.cu -- expert-ID matrix multiplication: the Direct route, the
+// routing map of the GroupedPrefill route, and the FFMA grouped GEMM used
+// for weight dtypes the tensor-core grouped kernel does not take.
+//
+// Semantics: mlx-native 0.13.0, src/ops/dense_matmul_id.rs -- module
+// contract (a strided stack of row-major [n, k] expert matrices, f32
+// activations, f32 output), `dense_matmul_id` (input token/slot strides per
+// layout; an id outside n_experts gives a zero output row without forming a
+// weight address), `DenseMatmulIdScratch` (expert_counts, routed_rows).
+//
+// Direct route.  The pages launch one thread group per (8 outputs, routed
+// row).  Here a CTA owns (routed row r, a tile of 32 expert rows j).  The
+// routed rows are cut into windows of 256; the CTA of the FIRST routed row
+// in a window that selects expert e computes every row of that window that
+// selects e, and the CTAs of later rows with the same expert exit at once.
+// So each distinct expert of a window is streamed from HBM once, whatever
+// the number of tokens that picked it.  Rows of W are read as coalesced
+// 16-byte vectors (L1 bypassed), activations through L1.
+//
+// Routing map.  One CTA of 32 warps builds expert_counts and routed_rows
+// without atomics: each warp owns a contiguous segment of routed rows,
+// counts it per expert with __match_any_sync (one leader lane per distinct
+// id updates the warp's private counter row in shared memory), the per
+// expert counts are scanned across warps in row order, and a second pass
+// scatters every row index to its final, ascending position.  Extra CTAs of
+// the same launch zero-fill output rows whose id is out of range.
+#include "device_common.cuh"
+
+namespace gbmm {
+
+namespace {
+
+constexpr int kDirectThreads = 256;
+constexpr int kDirectRows = 32;     // expert rows (outputs j) per CTA
+constexpr int kDirectWindow = 256;  // routed rows searched for sharers (== threads)
+constexpr int kDirectXR = 4;        // routed rows per pass over the W tile
+constexpr int kDirectUnroll = 8;    // 16-byte W vectors in flight per lane
+
+__device__ __forceinline__ const float *x_row(const MatmulIdParams &p, uint32_t r) {
+    const int64_t t = r / p.top_k;
+    const int64_t s = r % p.top_k;
+    return p.x + t * p.x_token_stride + s * p.x_slot_stride;
+}
+
+template <typename TW>
+__global__ void __launch_bounds__(kDirectThreads)
+matmul_id_direct_kernel(MatmulIdParams p, int vec_ok) {
+    constexpr int V = Elem<TW>::kVec;
+    __shared__ uint32_t s_list[kDirectWindow];
+    __shared__ int s_warp_cnt[kDirectThreads / 32];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    for (int64_t r = blockIdx.x; r < p.total_rows; r += gridDim.x) {
+        for (int64_t jt = blockIdx.y; jt * kDirectRows < p.n; jt += gridDim.y) {
+            const int64_t j0 = jt * kDirectRows;
+            const int64_t j1 = j0 + kDirectRows < p.n ? j0 + kDirectRows : p.n;
+            const uint32_t e = p.ids[r];
+            if (e >= static_cast<uint32_t>(p.n_experts)) {
+                for (int64_t j = j0 + tid; j < j1; j += blockDim.x) p.out[r * p.n + j] = 0.f;
+                continue;
+            }
+            const int64_t w0 = (r / kDirectWindow) * kDirectWindow;
+            const int64_t w1 = w0 + kDirectWindow < p.total_rows ? w0 + kDirectWindow : p.total_rows;
+            const int64_t rr = w0 + tid;
+            const uint32_t my_e = rr < w1 ? p.ids[rr] : 0xffffffffu;
+            // an earlier row of the window selected the same expert: it owns the work
+            if (__syncthreads_or(rr < r && my_e == e)) continue;
+            const bool mine = rr >= r && rr < w1 && my_e == e;
+            const unsigned bal = __ballot_sync(0xffffffffu, mine);
+            if (lane == 0) s_warp_cnt[warp] = __popc(bal);
+            __syncthreads();
+            int off = 0, total = 0;
+            for (int w = 0; w < kDirectThreads / 32; ++w) {
+                if (w < warp) off += s_warp_cnt[w];
+                total += s_warp_cnt[w];
+            }
+            if (mine) s_list[off + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint32_t>(rr);
+            __syncthreads();
+
+            const TW *W = static_cast<const TW *>(p.w) + static_cast<int64_t>(e) * p.expert_stride_elems;
+            for (int l0 = 0; l0 < total; l0 += kDirectXR) {
+                const int nr = total - l0 < kDirectXR ? total - l0 : kDirectXR;
+                const float *xr[kDirectXR];
+                uint32_t orow[kDirectXR];
+#pragma unroll
+                for (int q = 0; q < kDirectXR; ++q) {
+                    orow[q] = s_list[l0 + (q < nr ? q : 0)];
+                    xr[q] = x_row(p, orow[q]);
+                }
+                for (int64_t j = j0 + warp; j < j1; j += kDirectThreads / 32) {
+                    const TW *wrow = W + j * p.k;
+                    float acc[kDirectXR];
+#pragma unroll
+                    for (int q = 0; q < kDirectXR; ++q) acc[q] = 0.f;
+                    int64_t x_done = 0;
+                    if (vec_ok) {
+                        const int64_t nch = p.k / V;
+                        int64_t c0 = 0;
+                        for (; c0 + 32 * kDirectUnroll <= nch; c0 += 32 * kDirectUnroll) {
+                            uint4 wv[kDirectUnroll];
+#pragma unroll
+                            for (int u = 0; u < kDirectUnroll; ++u)
+                                wv[u] = ld_stream16(wrow + (c0 + u * 32 + lane) * V);
+#pragma unroll
+                            for (int u = 0; u < kDirectUnroll; ++u) {
+                                float wf[V];
+                                unpack16<TW>(wv[u], wf);
+                                const int64_t xo = (c0 + u * 32 + lane) * V;
+#pragma unroll
+                                for (int q = 0; q < kDirectXR; ++q) {
+                                    if (q < nr) {
+#pragma unroll
+                                        for (int h = 0; h < V / 4; ++h) {
+                                            const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr[q] + xo) + h);
+                                            acc[q] = fmaf(wf[4 * h + 0], xv.x, acc[q]);
+                                            acc[q] = fmaf(wf[4 * h + 1], xv.y, acc[q]);
+                                            acc[q] = fmaf(wf[4 * h + 2], xv.z, acc[q]);
+                                            acc[q] = fmaf(wf[4 * h + 3], xv.w, acc[q]);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                        for (int64_t c = c0 + lane; c < nch; c += 32) {
+                            float wf[V];
+                            unpack16<TW>(ld_stream16(wrow + c * V), wf);
+#pragma unroll
+                            for (int q = 0; q < kDirectXR; ++q) {
+                                if (q < nr) {
+#pragma unroll
+                                    for (int h = 0; h < V / 4; ++h) {
+                                        const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr[q] + c * V) + h);
+                                        acc[q] = fmaf(wf[4 * h + 0], xv.x, acc[q]);
+                                        acc[q] = fmaf(wf[4 * h + 1], xv.y, acc[q]);
+                                        acc[q] = fmaf(wf[4 * h + 2], xv.z, acc[q]);
+                                        acc[q] = fmaf(wf[4 * h + 3], xv.w, acc[q]);
+                                    }
+                                }
+                            }
+                        }
+                        x_done = nch * V;
+                    }
+                    for (int64_t x = x_done + lane; x < p.k; x += 32) {
+                        const float wv = Elem<TW>::to_f(wrow[x]);
+#pragma unroll
+                        for (int q = 0; q < kDirectXR; ++q)
+                            if (q < nr) acc[q] = fmaf(wv, xr[q][x], acc[q]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kDirectXR; ++q) acc[q] = warp_sum(acc[q]);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int q = 0; q < kDirectXR; ++q)
+                            if (q < nr) p.out[static_cast<int64_t>(orow[q]) * p.n + j] = acc[q];
+                    }
+                }
+            }
+            __syncthreads();  // s_list / s_warp_cnt are rewritten by the next (r, jt)
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// routing map
+// ---------------------------------------------------------------------------
+
+constexpr int kMapThreads = 1024;
+constexpr int kMapWarps = kMapThreads / 32;
+constexpr int kMapBatch = 16;  // ids per lane held in registers per step
+
+__global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdParams p) {
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t E = static_cast<uint32_t>(p.n_experts);
+    const int64_t total = p.total_rows;
+
+    if (blockIdx.x > 0) {
+        // zero-fill output rows whose id is outside [0, n_experts)
+        __shared__ uint32_t s_rows[kMapThreads];
+        __shared__ int s_wc[kMapWarps];
+        for (int64_t base = static_cast<int64_t>(blockIdx.x - 1) * kMapThreads; base < total;
+             base += static_cast<int64_t>(gridDim.x - 1) * kMapThreads) {
+            const int64_t r = base + tid;
+            const bool bad = r < total && p.ids[r] >= E;
+            const unsigned bal = __ballot_sync(0xffffffffu, bad);
+            if (lane == 0) s_wc[warp] = __popc(bal);
+            __syncthreads();
+            int off = 0, cnt = 0;
+            for (int w = 0; w < kMapWarps; ++w) {
+                if (w < warp) off += s_wc[w];
+                cnt += s_wc[w];
+            }
+            if (bad) s_rows[off + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint32_t>(r);
+            __syncthreads();
+            for (int q = 0; q < cnt; ++q) {
+                float *orow = p.out + static_cast<int64_t>(s_rows[q]) * p.n;
+                for (int64_t j = tid; j < p.n; j += kMapThreads) orow[j] = 0.f;
+            }
+            __syncthreads();
+        }
+        return;
+    }
+
+    extern __shared__ uint32_t cnt[];  // [kMapWarps][E]
+    uint32_t *mine = cnt + static_cast<int64_t>(warp) * E;
+    int64_t seg = (total + kMapWarps - 1) / kMapWarps;
+    seg = (seg + 31) / 32 * 32;
+    const int64_t beg = static_cast<int64_t>(warp) * seg;
+    const int64_t end = beg + seg < total ? beg + seg : total;
+    for (uint32_t e = lane; e < E; e += 32) mine[e] = 0;
+    __syncwarp();
+
+    // pass 1: per-warp counts
+    for (int64_t base = beg; base < end; base += 32 * kMapBatch) {
+        uint32_t v[kMapBatch];
+#pragma unroll
+        for (int b = 0; b < kMapBatch; ++b) {
+            const int64_t r = base + b * 32 + lane;
+            v[b] = r < end ? p.ids[r] : 0xffffffffu;
+        }
+#pragma unroll
+        for (int b = 0; b < kMapBatch; ++b) {
+            const uint32_t key = v[b] < E ? v[b] : 0xffffffffu;
+            const unsigned grp = __match_any_sync(0xffffffffu, key);
+            if (key != 0xffffffffu && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    // exclusive scan across warps (row order) per expert; totals are the counts
+    for (uint32_t e = tid; e < E; e += kMapThreads) {
+        uint32_t run = 0;
+        for (int w = 0; w < kMapWarps; ++w) {
+            const uint32_t c = cnt[static_cast<int64_t>(w) * E + e];
+            cnt[static_cast<int64_t>(w) * E + e] = run;
+            run += c;
+        }
+        p.counts[e] = run;
+    }
+    __syncthreads();
+
+    // pass 2: scatter row indices to their ascending positions
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int64_t base = beg; base < end; base += 32 * kMapBatch) {
+        uint32_t v[kMapBatch];
+#pragma unroll
+        for (int b = 0; b < kMapBatch; ++b) {
+            const int64_t r = base + b * 32 + lane;
+            v[b] = r < end ? p.ids[r] : 0xffffffffu;
+        }
+#pragma unroll
+        for (int b = 0; b < kMapBatch; ++b) {
+            const int64_t r = base + b * 32 + lane;
+            const uint32_t key = v[b] < E ? v[b] : 0xffffffffu;
+            const unsigned grp = __match_any_sync(0xffffffffu, key);
+            if (key != 0xffffffffu) {
+                const uint32_t pos = mine[key] + __popc(grp & lt_mask);
+                if (pos < static_cast<uint32_t>(p.m))
+                    p.routed_rows[static_cast<int64_t>(key) * p.m + pos] = static_cast<uint32_t>(r);
+            }
+            __syncwarp();
+            if (key != 0xffffffffu && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
+            __syncwarp();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// grouped GEMM on the FFMA pipe (any weight dtype)
+// ---------------------------------------------------------------------------
+
+constexpr int kGM = 64;
+constexpr int kGN = 64;
+constexpr int kGK = 16;
+
+template <typename TW>
+__global__ void __launch_bounds__(256) matmul_id_grouped_simt_kernel(MatmulIdParams p) {
+    __shared__ float As[kGK][kGM + 4];
+    __shared__ float Bs[kGK][kGN + 4];
+    __shared__ uint32_t s_rows[kGM];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int64_t e = blockIdx.z;
+    const uint32_t cnt_raw = p.counts[e];
+    const int64_t cnt = cnt_raw < static_cast<uint32_t>(p.m) ? cnt_raw : p.m;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kGM;
+    if (i0 >= cnt) return;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kGN;
+    if (tid < kGM) s_rows[tid] = i0 + tid < cnt ? p.routed_rows[e * p.m + i0 + tid] : 0xffffffffu;
+    __syncthreads();
+    const TW *W = static_cast<const TW *>(p.w) + e * p.expert_stride_elems;
+    float acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+
+    for (int64_t k0 = 0; k0 < p.k; k0 += kGK) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * 256;
+            const int x = idx % kGK;
+            const int i = idx / kGK;
+            const uint32_t rr = s_rows[i];
+            float v = 0.f;
+            if (rr != 0xffffffffu && k0 + x < p.k) v = x_row(p, rr)[k0 + x];
+            As[x][i] = v;
+            const int64_t gj = n0 + i;  // reuse the mapping for B rows (64 of them)
+            float w = 0.f;
+            if (gj < p.n && k0 + x < p.k) w = Elem<TW>::to_f(W[gj * p.k + k0 + x]);
+            Bs[x][i] = w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int x = 0; x < kGK; ++x) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) av[r] = As[x][ty + 16 * r];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) bv[c] = Bs[x][tx + 16 * c];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const uint32_t rr = s_rows[ty + 16 * r];
+        if (rr == 0xffffffffu) continue;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int64_t gj = n0 + tx + 16 * c;
+            if (gj < p.n) p.out[static_cast<int64_t>(rr) * p.n + gj] = acc[r][c];
+        }
+    }
+}
+
+int sm_count() {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v > 0 ? v : 1;
+}
+
+template <typename TW>
+cudaError_t direct_t(const MatmulIdParams &p, int vec_ok, cudaStream_t s) {
+    const int64_t gx = p.total_rows < 0x7fffffffLL ? p.total_rows : 0x7fffffffLL;
+    const int64_t tiles = (p.n + kDirectRows - 1) / kDirectRows;
+    const int64_t gy = tiles < 65535 ? tiles : 65535;
+    matmul_id_direct_kernel<TW><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
+                                   kDirectThreads, 0, s>>>(p, vec_ok);
+    return cudaGetLastError();
+}
+
+template <typename TW>
+cudaError_t grouped_simt_t(const MatmulIdParams &p, cudaStream_t s) {
+    const int64_t gx = (p.m + kGM - 1) / kGM;
+    const int64_t gy = (p.n + kGN - 1) / kGN;
+    if (gx > 0x7fffffffLL || gy > 65535 || p.n_experts > 65535) return cudaErrorInvalidConfiguration;
+    matmul_id_grouped_simt_kernel<TW><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                                             static_cast<unsigned>(p.n_experts)),
+                                        256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream_t s) {
+    // 16-byte vectors need 16-byte aligned expert rows and activation rows
+    const int size = dtype_size(wdt);
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(p.w) % 16 == 0) &&
+                        ((p.expert_stride_elems * size) % 16 == 0) && ((p.k * size) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(p.x) % 16 == 0) &&
+                        ((p.x_token_stride * 4) % 16 == 0) && ((p.x_slot_stride * 4) % 16 == 0);
+    switch (wdt) {
+    case kF32: return direct_t<float>(p, vec_ok, s);
+    case kF16: return direct_t<__half>(p, vec_ok, s);
+    case kBF16: return direct_t<__nv_bfloat16>(p, vec_ok, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(kMapWarps) * static_cast<size_t>(p.n_experts) * 4;
+    static unsigned long long attr_set = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(matmul_id_map_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kMapWarps * 1024 * 4);
+        if (e != cudaSuccess) return e;
+        attr_set |= bit;
+    }
+    int64_t zero_ctas = (p.total_rows + kMapThreads - 1) / kMapThreads;
+    const int64_t cap = 2LL * sm_count();
+    if (zero_ctas > cap) zero_ctas = cap;
+    if (zero_ctas < 1) zero_ctas = 1;
+    matmul_id_map_kernel<<<static_cast<unsigned>(1 + zero_ctas), kMapThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s) {
+    switch (wdt) {
+    case kF32: return grouped_simt_t<float>(p, s);
+    case kF16: return grouped_simt_t<__half>(p, s);
+    case kBF16: return grouped_simt_t<__nv_bfloat16>(p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbmm

@@ -1,0 +1,287 @@
+"""GPU parity of the dense GEMM / GEMV entry points against the CPU oracle,
+called through the C ABI (gbmm_gemm / gbmm_gemv).
+
+Covers every route (tensor-core GEMM, FFMA GEMM, row/column GEMV, the
+skinny/wide path, the k == 0 fill), all dtypes and transposes, padded
+leading dims, batch strides (including broadcast), byte offsets, ragged
+tails, guard bands around C, and the three dense workloads at full size
+(the 4 x 4096^3 GEMM on sampled outputs).
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from gemv_moe_expert_gb300 import binding as gb  # noqa: E402
+from gemv_moe_expert_gb300 import synth  # noqa: E402
+from tests.gpu_util import (DevBuf, StridedGemm, NP_DT, assert_close, to_f64)  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+    torch.cuda.init()
+
+
+def run_case(oracle_mod, g: StridedGemm, fn=gb.gbmm_gemm, expect_kernel=None, idx=None):
+    a, b, c = g.device()
+    gb.gbmm_test_reset_launch_count()
+    st = fn(*g.args(a, b, c))
+    assert st == gb.GBMM_OK, gb.gbmm_last_error()
+    torch.cuda.synchronize()
+    if expect_kernel is not None:
+        assert gb.gbmm_test_last_kernel() == expect_kernel
+        assert gb.gbmm_test_launch_count() == 1
+    assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+    assert a.guards_intact() and b.guards_intact() and c.guards_intact()
+    assert g.c_gaps_untouched(c)
+    got = g.gather_c(c)
+    if idx is None:
+        ref, ref_abs = g.oracle(oracle_mod)
+        return assert_close(got, ref, ref_abs, g.dtype, g.dtype, f"{g.dtype} {g.m}x{g.n}x{g.k}")
+    ref, ref_abs = g.oracle(oracle_mod, idx=idx)
+    return assert_close(got.reshape(-1)[idx], ref, ref_abs, g.dtype, g.dtype, "sampled")
+
+
+# ---------------------------------------------------------------------------
+# worked examples printed on the tract-metal page
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+def test_worked_examples(oracle_mod, dtype):
+    b, m, n, k = 2, 2, 4, 3
+    a = synth._store(np.arange(b * m * k, dtype=np.float32), dtype)
+    bb = synth._store(np.arange(b * k * n, dtype=np.float32), dtype)
+    da, db, dc = DevBuf(a.nbytes, host=a), DevBuf(bb.nbytes, host=bb), DevBuf(b * m * n * a.itemsize)
+    st = gb.gbmm_gemm(dtype, b, m, n, k, 0, 0, da.ptr, 0, k, m * k, db.ptr, 0, n, k * n, dc.ptr, 0,
+                      n, m * n)
+    assert st == gb.GBMM_OK, gb.gbmm_last_error()
+    got = to_f64(dc.read(NP_DT[dtype], b * m * n), dtype)
+    expect = np.array([20, 23, 26, 29, 56, 68, 80, 92, 344, 365, 386, 407, 488, 518, 548, 578],
+                      dtype=np.float64)
+    if dtype == "bf16":
+        # 8 significant bits: the printed values, rounded to bf16
+        expect = to_f64(synth.f32_to_bf16_bits(expect.astype(np.float32)), "bf16")
+    assert np.array_equal(got, expect)
+    # all ones, b=10 m=n=32 k=16 -> 16 everywhere
+    g = StridedGemm(dtype, 10, 32, 32, 16, False, False, dist="ints")
+    g.a[:] = synth._store(np.ones(g.a.size, np.float32), dtype)
+    g.b[:] = synth._store(np.ones(g.b.size, np.float32), dtype)
+    da, db, dc = g.device()
+    assert gb.gbmm_gemm(*g.args(da, db, dc)) == gb.GBMM_OK
+    assert np.all(g.gather_c(dc) == 16.0)
+
+
+# ---------------------------------------------------------------------------
+# tensor-core GEMM (f16/bf16, A [m,k], B stored [n,k])
+# ---------------------------------------------------------------------------
+
+TC_SHAPES = [
+    (1, 128, 256, 64),        # exactly one tile, one k-block
+    (2, 200, 300, 150),       # ragged m, n and k tails, several tiles
+    (1, 257, 513, 1000),      # one past the tile edges
+    (3, 384, 256, 4096),      # long k
+    (1, 1000, 40, 72),        # narrow n
+    (1, 16, 1000, 520),       # m = 16 (just above the skinny path)
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=[str(s) for s in TC_SHAPES])
+def test_tc_gemm_parity(oracle_mod, dtype, shape):
+    batch, m, n, k = shape
+    g = StridedGemm(dtype, batch, m, n, k, False, True, std=1.0 / np.sqrt(k), seed=batch + m)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_gemm_strides_offsets_broadcast(oracle_mod, dtype):
+    # padded leading dims (multiples of 8 elements), batch strides with gaps,
+    # 16-byte aligned byte offsets, and a broadcast A (stride 0)
+    g = StridedGemm(dtype, 3, 130, 270, 200, False, True, lda=208, ldb=264, ldc=300,
+                    sa=0, sb=270 * 264 + 64, sc=130 * 300 + 8, a_off=32, b_off=64, c_off=16)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+    # unaligned C (ldc odd) takes the scalar store path of the same kernel
+    g = StridedGemm(dtype, 2, 129, 257, 64, False, True, ldc=259, c_off=2)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_gemm_exact_small_integers(oracle_mod, dtype):
+    # |v| <= 8 integers, k = 1024: every product and partial sum is an exact
+    # integer in f32 and every |C| <= 65536; check exact agreement where the
+    # output dtype represents the value exactly
+    g = StridedGemm(dtype, 1, 256, 512, 1024, False, True, dist="ints")
+    a, b, c = g.device()
+    assert gb.gbmm_gemm(*g.args(a, b, c)) == gb.GBMM_OK
+    got = g.gather_c(c)
+    ref, _ = g.oracle(oracle_mod)
+    rounded = to_f64(synth._store(ref.astype(np.float32).reshape(-1), dtype), dtype).reshape(ref.shape)
+    assert np.array_equal(got, rounded)
+
+
+# ---------------------------------------------------------------------------
+# FFMA GEMM: f32, and the f16/bf16 layouts the tensor-core path does not take
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+@pytest.mark.parametrize("ta,tb", [(False, False), (False, True), (True, False), (True, True)])
+def test_general_gemm_parity(oracle_mod, dtype, ta, tb):
+    g = StridedGemm(dtype, 2, 70, 90, 45, ta, tb, lda=(70 if ta else 45) + 3,
+                    ldb=(45 if tb else 90) + 5, ldc=95, a_off=synth.ITEMSIZE[dtype] * 3)
+    # the odd offsets and leading dims rule out the TMA path for every dtype
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+
+
+def test_f32_gemm_workload_c1(oracle_mod):
+    """Single f32 GEMM 64x64x128, NN, U[-1,1], seed 0: every output."""
+    w = synth.workload("c1_f32_gemm")
+    g = StridedGemm("f32", 1, 64, 64, 128, False, False)
+    g.a[:] = w.a.reshape(-1)
+    g.b[:] = w.b.reshape(-1)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+
+
+def test_f32_gemm_page_shapes(oracle_mod):
+    # the pages' f32 matmul shapes, both readings of the tuple order
+    for (bb, m, x, y), tb in [((1, 3, 5, 4), False), ((1, 2, 5, 10), True), ((1, 4, 4, 4), True),
+                              ((1, 4, 4, 200), True), ((1, 25, 1280, 32000), True)]:
+        for (n, k) in ((x, y), (y, x)):
+            g = StridedGemm("f32", bb, m, n, k, False, tb, std=1.0, seed=m)
+            run_case(oracle_mod, g)
+
+
+# ---------------------------------------------------------------------------
+# GEMV (m == 1 or n == 1) and the skinny/wide path
+# ---------------------------------------------------------------------------
+
+GEMV_CASES = [
+    # (batch, m, n, k, ta, tb)
+    (1, 1, 11, 300, False, True),     # row-dot over B, ragged k
+    (1, 1, 700, 1031, False, False),  # column-dot over B
+    (3, 1, 129, 64, True, True),      # strided vector (ta)
+    (2, 333, 1, 520, False, False),   # row-dot over A, strided vector (B column)
+    (2, 77, 1, 999, True, True),      # column-dot over A
+    (1, 1, 1, 4097, False, True),     # a dot product
+    (10, 1, 4, 4, False, False),      # the pages' mat-vec shapes
+    (1, 4, 1, 4, False, False),
+    (5, 1, 7, 15, False, True),
+    (5, 1, 15, 7, False, True),
+    (1, 1, 64, 65536, False, False),  # few outputs, long k: split-k over a cluster
+]
+
+
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+@pytest.mark.parametrize("case", GEMV_CASES, ids=[str(c) for c in GEMV_CASES])
+@pytest.mark.parametrize("entry", ["gemv", "gemm"])
+def test_gemv_parity(oracle_mod, dtype, case, entry):
+    batch, m, n, k, ta, tb = case
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, std=1.0, seed=k)
+    fn = gb.gbmm_gemv if entry == "gemv" else gb.gbmm_gemm
+    ratio = run_case(oracle_mod, g, fn=fn)
+    assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_rowdot", "gbmm_gemv_coldot")
+    assert ratio <= 1.0
+
+
+def test_gemv_decode_workload_c2(oracle_mod):
+    """Decode GEMV f16: x [1,4096] ~N(0,1), W [11008,4096] ~N(0,0.02) (tb): all outputs."""
+    w = synth.workload("c2_f16_gemv")
+    g = StridedGemm("f16", 1, 1, 11008, 4096, False, True)
+    g.a[:] = w.a.reshape(-1)
+    g.b[:] = w.b.reshape(-1)
+    run_case(oracle_mod, g, fn=gb.gbmm_gemv, expect_kernel="gbmm_gemv_rowdot")
+
+
+def _wide_shapes():
+    out = []
+    with open(os.path.join(GOLDEN, "gemv_wide_gate_shapes.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                dt, m, n, k = line.split()
+                out.append((dt, int(m), int(n), int(k)))
+    return out
+
+
+@pytest.mark.parametrize("dtype,m,n,k", _wide_shapes())
+def test_wide_skinny_ramp(oracle_mod, dtype, m, n, k):
+    """x [m,k] against w [n,k] with the pages' ramp inputs (exact in f32)."""
+    g = StridedGemm(dtype, 1, m, n, k, False, True)
+    g.a[:] = synth.ramp((m * k,), 1, dtype)
+    g.b[:] = synth.ramp((n * k,), 2, dtype)
+    run_case(oracle_mod, g)
+    if dtype != "f32":
+        assert gb.gbmm_test_last_kernel() == "gbmm_gemv_rowdot"
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("m", list(range(2, 16)))
+def test_wide_skinny_random(oracle_mod, dtype, m):
+    g = StridedGemm(dtype, 1, m, 256 + 3, 4096 + 8, False, True, lda=4096 + 16, ldc=300, seed=m)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_rowdot")
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+def test_k_zero_writes_zeros(oracle_mod, dtype):
+    g = StridedGemm(dtype, 2, 5, 7, 0, False, False, ldc=9, sc=60)
+    a, b, c = g.device()
+    assert gb.gbmm_gemm(*g.args(a, b, c)) == gb.GBMM_OK
+    assert gb.gbmm_test_last_kernel() == "gbmm_fill_zero"
+    assert np.all(g.gather_c(c) == 0.0)
+    assert g.c_gaps_untouched(c) and c.guards_intact()
+
+
+def test_empty_problems_launch_nothing():
+    g = StridedGemm("f16", 1, 0, 7, 9, False, True)
+    a, b, c = g.device()
+    gb.gbmm_test_reset_launch_count()
+    assert gb.gbmm_gemm(*g.args(a, b, c)) == gb.GBMM_OK
+    assert gb.gbmm_test_launch_count() == 0
+    assert c.guards_intact()
+
+
+def test_batched_gemm_workload_c3_sampled(oracle_mod):
+    """Batched f16 GEMM 4 x 4096^3, B stored [b,N,K], ~N(0,1/64): 4096 sampled
+    outputs (all corners, tile edges and random) against the oracle."""
+    w = synth.workload("c3_f16_gemm")
+    b, m, n, k = 4, 4096, 4096, 4096
+    da, db = DevBuf(w.a.nbytes, host=w.a), DevBuf(w.b.nbytes, host=w.b)
+    dc = DevBuf(b * m * n * 2)
+    st = gb.gbmm_gemm("f16", b, m, n, k, 0, 1, da.ptr, 0, k, m * k, db.ptr, 0, k, n * k, dc.ptr, 0,
+                      n, m * n)
+    assert st == gb.GBMM_OK, gb.gbmm_last_error()
+    assert gb.gbmm_test_last_kernel() == "gbmm_gemm_tc"
+    torch.cuda.synchronize()
+    assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+    assert dc.guards_intact()
+    rng = np.random.default_rng(1)
+    pts = [(bi, i, j) for bi in range(b) for i in (0, 127, 128, m - 1) for j in (0, 255, 256, n - 1)]
+    idx = [bi * m * n + i * n + j for bi, i, j in pts]
+    idx += list(rng.integers(0, b * m * n, 4096 - len(idx)))
+    idx = np.array(idx, dtype=np.int64)
+    ref, ref_abs = synth_oracle_gemm(oracle_mod, w, idx)
+    got = to_f64(dc.read(np.float16, b * m * n)[idx], "f16")
+    assert_close(got, ref, ref_abs, "f16", "f16", "c3 sampled")
+    # the full output is finite and not trivially zero
+    full = dc.read(np.float16, b * m * n)
+    assert np.isfinite(full).all() and np.count_nonzero(full) > 0.99 * full.size
+
+
+def synth_oracle_gemm(oracle_mod, w, idx):
+    return oracle_mod.gemm(w.dtype, w.batch, w.m, w.n, w.k, w.ta, w.tb, w.a.reshape(-1), w.lda,
+                           w.stride_a, w.b.reshape(-1), w.ldb, w.stride_b, idx=idx)

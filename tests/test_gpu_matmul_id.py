@@ -1,0 +1,190 @@
+"""GPU parity of gbmm_matmul_id (both routes) against the CPU oracle, called
+through the C ABI.  Routing maps (expert_counts, and each expert's routed
+rows) must be bit-exact; f32 outputs must meet the tolerance of the weight
+dtype (1e-5 * sum|a||b| for f32 weights, 2e-3 * sum|a||b| for f16/bf16).
+
+Semantics: mlx-native 0.13.0, src/ops/dense_matmul_id.rs.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from gemv_moe_expert_gb300 import binding as gb  # noqa: E402
+from gemv_moe_expert_gb300 import synth  # noqa: E402
+from tests.gpu_util import DevBuf, assert_close  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+    torch.cuda.init()
+
+
+class Run:
+    """Uploads a MatmulIdCase, calls gbmm_matmul_id, reads results back."""
+
+    def __init__(self, case: synth.MatmulIdCase, out_fill=0x7F):
+        self.case = case
+        c = case
+        self.params = gb.make_params(c.m, c.n, c.k, c.top_k, c.n_experts, c.expert_stride_bytes,
+                                     c.input_layout, c.multiplicity, c.route)
+        st, cap = gb.gbmm_matmul_id_capability(c.wdtype, self.params)
+        assert st == gb.GBMM_OK, gb.gbmm_last_error()
+        self.cap = cap
+        self.w = DevBuf(c.w.nbytes, host=c.w)
+        self.x = DevBuf(c.x.nbytes, host=c.x)
+        self.ids = DevBuf(c.ids.nbytes, host=c.ids)
+        # garbage in the output: every row must be fully overwritten
+        self.out = DevBuf(cap.required_output_bytes, fill=out_fill)
+        self.scratch = None
+        if c.route == gb.ROUTE_GROUPED_PREFILL:
+            self.counts = DevBuf(cap.expert_counts_bytes, fill=0xEE)
+            self.rows = DevBuf(cap.routed_rows_bytes, fill=0xEE)
+            self.scratch = gb.make_scratch(self.counts.ptr, cap.expert_counts_bytes, self.rows.ptr,
+                                           cap.routed_rows_bytes, c.n_experts, c.m)
+
+    def call(self):
+        c = self.case
+        gb.gbmm_test_reset_launch_count()
+        st, rec = gb.gbmm_matmul_id(self.params, c.wdtype, self.w.ptr, c.w.nbytes, self.x.ptr,
+                                    c.x.nbytes, self.ids.ptr, c.ids.nbytes, self.out.ptr,
+                                    self.cap.required_output_bytes, self.scratch)
+        assert st == gb.GBMM_OK, gb.gbmm_last_error()
+        torch.cuda.synchronize()
+        assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+        expect_launches = 2 if c.route == gb.ROUTE_GROUPED_PREFILL else 1
+        assert rec.launch_count == expect_launches and rec.route == c.route
+        assert rec.weight_dtype == gb.DTYPE_CODES[c.wdtype]
+        assert gb.gbmm_test_launch_count() == expect_launches
+        for buf in (self.w, self.x, self.ids, self.out):
+            assert buf.guards_intact()
+        if self.scratch is not None:
+            assert self.counts.guards_intact() and self.rows.guards_intact()
+        return self
+
+    def output(self):
+        c = self.case
+        return self.out.read(np.float32, c.m * c.top_k * c.n).astype(np.float64)
+
+    def check(self, oracle_mod, idx=None):
+        c = self.case
+        got = self.output()
+        ref, ref_abs = oracle_mod.matmul_id(c.wdtype, c.m, c.n, c.k, c.top_k, c.n_experts,
+                                            c.expert_stride_bytes, c.input_layout, c.w, c.x,
+                                            c.ids, idx=idx)
+        if idx is not None:
+            got = got[idx]
+        ratio = assert_close(got, ref, ref_abs, c.wdtype, "f32", c.name)
+        if self.scratch is not None:
+            self.check_map(oracle_mod)
+        return ratio
+
+    def check_map(self, oracle_mod):
+        c = self.case
+        counts_ref, rows_ref = oracle_mod.map_distinct(c.m, c.top_k, c.n_experts, c.ids)
+        counts = self.counts.read(np.uint32, c.n_experts)
+        assert np.array_equal(counts, counts_ref)
+        rows = self.rows.read(np.uint32, c.n_experts * c.m).reshape(c.n_experts, c.m)
+        for e in range(c.n_experts):
+            n_e = min(int(counts_ref[e]), c.m)
+            assert np.array_equal(rows[e, :n_e], rows_ref[e, :n_e]), e
+
+
+def test_direct_decode_workload_c4(oracle_mod):
+    """m=4, E=64, top_k=8 distinct uniform ids, k=2048, n=1408, bf16 W: every output."""
+    r = Run(synth.workload("c4_moe_direct")).call()
+    r.check(oracle_mod)
+
+
+def test_grouped_prefill_workload_c5_sampled(oracle_mod):
+    """m=4096, E=128, top_k=8 Zipf(1.1) ids, k=4096, n=1536, bf16 W: the routing map
+    bit-exact, and 8192 sampled outputs (first/last rows of every expert's list
+    and random) against the oracle."""
+    case = synth.workload("c5_moe_grouped")
+    r = Run(case).call()
+    c = case
+    counts_ref, rows_ref = oracle_mod.map_distinct(c.m, c.top_k, c.n_experts, c.ids)
+    r.check_map(oracle_mod)
+    rng = np.random.default_rng(5)
+    picks = []
+    for e in range(c.n_experts):
+        lst = rows_ref[e, :counts_ref[e]]
+        for rr in (lst[0], lst[-1], lst[len(lst) // 2]):
+            for j in (0, c.n - 1, int(rng.integers(0, c.n))):
+                picks.append(int(rr) * c.n + j)
+    total = c.m * c.top_k * c.n
+    picks += list(rng.integers(0, total, 8192 - len(picks)))
+    idx = np.array(picks, dtype=np.int64)
+    got = r.output()
+    ref, ref_abs = oracle_mod.matmul_id(c.wdtype, c.m, c.n, c.k, c.top_k, c.n_experts,
+                                        c.expert_stride_bytes, c.input_layout, c.w, c.x, c.ids,
+                                        idx=idx)
+    assert_close(got[idx], ref, ref_abs, "bf16", "f32", "c5 sampled")
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("wdtype", synth.DTYPES)
+@pytest.mark.parametrize("route", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_matmul_id_parity_small(oracle_mod, wdtype, route, layout):
+    # several tiles in every dimension, ragged tails, padded expert stride
+    case = synth.matmul_id_case(f"{wdtype}-r{route}-l{layout}", wdtype, 150, 300, 520, 4, 12,
+                                route=route, input_layout=layout, stride_pad_elems=8, seed=3)
+    Run(case).call().check(oracle_mod)
+
+
+@pytest.mark.parametrize("route", [0, 1])
+def test_out_of_range_ids_give_zero_rows(oracle_mod, route):
+    m, top_k, E = 40, 4, 9
+    ids = synth.distinct_ids(m, top_k, E, seed=8)
+    ids[3, 1] = E
+    ids[7, 0] = 0xFFFFFFFF
+    ids[7, 3] = 1000
+    ids[39, 2] = E + 1
+    case = synth.matmul_id_case("oob", "bf16", m, 72, 136, top_k, E, route=route, ids=ids)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    out = r.output().reshape(m, top_k, -1)
+    for t, s in [(3, 1), (7, 0), (7, 3), (39, 2)]:
+        assert np.all(out[t, s] == 0.0)
+
+
+def test_direct_may_repeat(oracle_mod):
+    case = synth.matmul_id_case("repeat", "bf16", 6, 200, 264, 5, 3, route=0, multiplicity=1,
+                                seed=2)
+    Run(case).call().check(oracle_mod)
+
+
+def test_direct_many_windows(oracle_mod):
+    # 800 routed rows: several 256-row sharing windows, experts shared across tokens
+    case = synth.matmul_id_case("windows", "f16", 100, 96, 512, 8, 16, route=0, seed=6)
+    Run(case).call().check(oracle_mod)
+
+
+def test_grouped_scratch_reuse_two_calls(oracle_mod):
+    """Two grouped calls in a row on the same scratch with different ids: the
+    second map overwrites the first in stream order."""
+    case = synth.matmul_id_case("reuse", "bf16", 64, 128, 256, 4, 10, route=1, seed=1)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    ids2 = synth.distinct_ids(64, 4, 10, seed=99)
+    r.case.ids = ids2
+    r.ids.t[4096:4096 + ids2.nbytes].copy_(torch.from_numpy(ids2.view(np.uint8).reshape(-1).copy()))
+    r.call().check(oracle_mod)
+
+
+def test_grouped_all_rows_one_expert(oracle_mod):
+    # every token selects expert 0 in slot 0: one expert's list holds all m rows
+    m, top_k, E = 300, 2, 4
+    ids = np.zeros((m, top_k), dtype=np.uint32)
+    ids[:, 1] = 1 + (np.arange(m) % 3)
+    case = synth.matmul_id_case("one-expert", "bf16", m, 160, 192, top_k, E, route=1, ids=ids)
+    Run(case).call().check(oracle_mod)
