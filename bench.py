@@ -255,6 +255,23 @@ class Problem:
             raise RuntimeError(f"{self.key}: {gb.gbmm_status_string(st)}: {gb.gbmm_last_error()}")
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest `value` over all ranks of the default process group (the value
+    itself without one).  Works with gloo (CPU tensors) and nccl (device)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def step_value(roof_total_s: float, world: int, ms_per_step: float) -> float:
+    """Whole-job % of one GB300's roofline: every rank runs one full step."""
+    return 100.0 * world * roof_total_s / (ms_per_step / 1e3)
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -331,12 +348,9 @@ def run_ours(args) -> None:
             per_call[k] += ev[s][i].elapsed_time(ev[s][i + 1])
     per_call = {k: v / args.steps for k, v in per_call.items()}
 
-    t_local = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t_local.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device="cuda")
     ms_per_step = elapsed_ms / args.steps
-    value = 100.0 * world * roof_total / (ms_per_step / 1e3)
+    value = step_value(roof_total, world, ms_per_step)
 
     # ---- end to end: pinned host inputs in, results out, every step ----
     e2e = None
@@ -376,12 +390,8 @@ def run_ours(args) -> None:
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1) / e2e_steps
-        t_e = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(t_e, op=dist.ReduceOp.MAX)
-        e_ms = float(t_e.item())
-        e2e = {"value": 100.0 * world * roof_total / (e_ms / 1e3), "unit": UNIT,
+        e_ms = max_over_ranks(s0.elapsed_time(s1) / e2e_steps, device="cuda")
+        e2e = {"value": step_value(roof_total, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms, "steps": e2e_steps}
 

@@ -552,10 +552,37 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
     if (!resolve("gbmm_matmul_id_grouped")) return GBMM_ERR_KERNEL_UNAVAILABLE;
     mp.counts = scratch->expert_counts;
     mp.routed_rows = scratch->routed_rows;
+    // tensor-core grouped GEMM: bf16 weights read by TMA (16-byte aligned base,
+    // expert stride and rows), 16-byte aligned activation rows
+    CUtensorMap map_w;
+    bool tc = weight_dtype == GBMM_BF16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
+              p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 && aligned(input, 16) &&
+              p->n_experts <= static_cast<uint32_t>(grouped_tc_max_experts());
+    if (tc) {
+        PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+        cuuint64_t dims[3] = {p->k, p->n, p->n_experts};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->k) * 2, p->expert_stride_bytes};
+        cuuint32_t box[3] = {64u, 256u, 1u};
+        cuuint32_t estr[3] = {1u, 1u, 1u};
+        tc = enc != nullptr &&
+             enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (tc) {
+        mp.err = device_error_word();
+        if (mp.err == nullptr) return fail(GBMM_ERR_CUDA, "%s: device error word unavailable", fn);
+    }
     st = after_launch(launch_matmul_id_map(mp, stream), "gbmm_matmul_id_map", stream);
     if (st != GBMM_OK) return st;
-    st = after_launch(launch_matmul_id_grouped_simt(weight_dtype, mp, stream), "gbmm_matmul_id_grouped",
-                      stream);
+    if (tc) {
+        const int out_vec_ok = aligned(out, 16) && p->n % 4 == 0;
+        st = after_launch(launch_matmul_id_grouped_tc(map_w, mp, out_vec_ok, device_sm_count(), stream),
+                          "gbmm_matmul_id_grouped_tc", stream);
+    } else {
+        st = after_launch(launch_matmul_id_grouped_simt(weight_dtype, mp, stream),
+                          "gbmm_matmul_id_grouped_simt", stream);
+    }
     if (st != GBMM_OK) return st;
     if (receipt) *receipt = gbmm_matmul_id_receipt{static_cast<uint32_t>(weight_dtype), p->route, 2};
     return GBMM_OK;

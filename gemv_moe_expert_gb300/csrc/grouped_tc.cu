@@ -1,0 +1,417 @@
+// grouped_tc.cu -- the grouped GEMM of the GroupedPrefill route on the sm_103a
+// tensor cores, for bf16 expert weights and f32 activations.
+//
+// Semantics: mlx-native 0.13.0, src/ops/dense_matmul_id.rs, `dense_matmul_id`
+// (GroupedPrefill: per expert, the routed rows listed by the map dispatch
+// times that expert's row-major [n, k] matrix, f32 output rows).
+//
+// For expert e and its routed rows r_0 < r_1 < ... (routed_rows[e*m + i],
+// i < expert_counts[e]) the kernel computes the GEMM
+//     out[r_i, j] = sum_x W_e[j, x] * xrow(r_i)[x]
+// with M = routed rows (gathered), N = n, K = k, in tiles of 128 rows x 256
+// outputs.  The activations are f32; tensor cores take bf16 pairs, so every
+// activation is split exactly as x = hi + lo with hi = bf16(x) and
+// lo = bf16(x - hi) and both halves are multiplied by the same bf16 weight
+// tile into one f32 accumulator.  The split leaves a relative error of at
+// most 2^-16 on each activation (against 2^-8 for a single bf16 rounding),
+// so the result stays an f32-accurate expert product.
+//
+// One persistent CTA per SM, 10 warps:
+//   warp 0     TMA: 256x64 bf16 weight tiles of W_e (3-D tensor map over
+//              (k, n, expert), 128-byte swizzle), streamed with L2 evict-first
+//   warp 1     TMEM allocation (two 128x256 f32 accumulators) and the MMA
+//              issuer: 8 x tcgen05.mma (M=128, N=256, K=16) per 64-wide k-block
+//   warps 2..5 epilogue: TMEM -> registers -> f32 rows of `out`, scattered to
+//              their routed rows (each thread writes 128 contiguous bytes)
+//   warps 6..9 activation producers: gather 128 routed x rows (f32, L2
+//              evict-last: each token row serves top_k experts), split into
+//              bf16 hi/lo, write the 128-byte-swizzled K-major smem layout the
+//              MMA descriptors expect, then arrive on the stage barrier.
+// Tile list: every CTA derives it from expert_counts (written by the map
+// launch before this one): tiles ordered by expert, then row block, then
+// output block.  Every mbarrier wait is bounded; see gemm_tc.cu.
+#include "device_common.cuh"
+
+namespace gbmm {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 3;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp0 = 6;
+constexpr uint32_t kXBytes = kBM * kBK * 2;  // one bf16 half of the activation tile
+constexpr uint32_t kWBytes = kBN * kBK * 2;
+constexpr uint32_t kStageBytes = 2 * kXBytes + kWBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxExperts = 1024;
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + (kMaxExperts + 8) * 4 + 256 + 1024;
+
+struct GroupedTile {
+    int e, mb, nb, rows;
+};
+
+// expert of tile t: the largest e with prefix[e] <= t (prefix has E+1 entries)
+__device__ __forceinline__ GroupedTile decode_grouped(int t, const uint32_t *prefix, int E, int nblk,
+                                                      const uint32_t *counts, int m) {
+    int lo = 0, hi = E;  // invariant prefix[lo] <= t < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= static_cast<uint32_t>(t)) lo = mid; else hi = mid;
+    }
+    GroupedTile g;
+    g.e = lo;
+    const int local = t - static_cast<int>(prefix[lo]);
+    g.mb = local / nblk;
+    g.nb = local % nblk;
+    const int cnt = min(static_cast<int>(counts[lo]), m);
+    g.rows = min(kBM, cnt - g.mb * kBM);
+    return g;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float bf16_lo_of(uint32_t packed, int half) {
+    return __uint_as_float(half ? (packed & 0xffff0000u) : (packed << 16));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams p, int out_vec_ok) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t s_base = raw_addr + pad;
+    // stage s: x_hi at s_base + s*kStageBytes, x_lo after it, then the weight tile
+    uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(prefix + kMaxExperts + 8);
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ uint32_t warp_tot[kThreads / 32];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = static_cast<int>(p.n_experts);
+    const int m = static_cast<int>(p.m);
+    const int nblk = static_cast<int>((p.n + kBN - 1) / kBN);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1 + 4);  // TMA arrive + one arrive per producer warp
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&map_w);
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+
+    // tile prefix over experts: prefix[e] = sum_{e' < e} ceil(count/128) * nblk
+    {
+        constexpr int kPer = 4;  // 320 threads x 4 >= 1024 + 1 entries
+        uint32_t v[kPer];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = threadIdx.x * kPer + q;
+            uint32_t t = 0;
+            if (e < E) {
+                const uint32_t c = min(p.counts[e], static_cast<uint32_t>(m));
+                t = (c + kBM - 1) / kBM * static_cast<uint32_t>(nblk);
+            }
+            v[q] = t;
+            sum += t;
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        uint32_t base = 0;
+        for (int w = 0; w < warp; ++w) base += warp_tot[w];
+        uint32_t run = base + incl - sum;  // exclusive prefix of this thread's first entry
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = threadIdx.x * kPer + q;
+            if (e <= E) prefix[e] = run;
+            run += v[q];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = static_cast<int>(prefix[E]);
+    const int kblocks = static_cast<int>((p.k + kBK - 1) / kBK);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- weight tiles (TMA) ----------------
+            const uint64_t pol = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), kWBytes);
+                    tma_load_3d_hint(s_base + stage * kStageBytes + 2 * kXBytes, &map_w, full_bar(stage),
+                                     kb * kBK, g.nb * kBN, g.e, pol);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report_device_error(p.err, kKidGroupedTc);
+                // the stage barriers also count producer-warp arrivals, so wait on
+                // the bytes only: each issued copy completes its own transaction
+                for (int s = 0; s < kStages; ++s) {
+                    const uint32_t n_s = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
+                    if (n_s > 0) mbar_wait_bounded(full_bar(s), (n_s - 1u) & 1u, p.wait_limit_ns, nullptr);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t kIdesc = idesc_f16(1u, kBM, kBN);  // bf16 x bf16 -> f32
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t s_hi = s_base + stage * kStageBytes;
+                    const uint32_t s_lo = s_hi + kXBytes;
+                    const uint32_t s_w = s_hi + 2 * kXBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t dw = sdesc_kmajor_sw128(s_w + kk * 32);
+                        umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_hi + kk * 32), dw, kIdesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_lo + kk * 32), dw, kIdesc, 1u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report_device_error(p.err, kKidGroupedTc);
+            }
+            umma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, nullptr);
+        }
+    } else if (warp < kProducerWarp0) {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
+            int ready = 0;
+            if (lane == 0) ready = mbar_wait_bounded(tfull_bar(acc), acc_phase, p.wait_limit_ns, abort_flag);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    report_device_error(p.err, kKidGroupedTc);
+                }
+                break;
+            }
+            __syncwarp();
+            tc_fence_after();
+            const int i = quarter * 32 + lane;
+            const bool valid = i < g.rows;
+            const int64_t r = valid ? static_cast<int64_t>(p.routed_rows[static_cast<int64_t>(g.e) * m +
+                                                                         g.mb * kBM + i])
+                                    : 0;
+            float *orow = p.out + r * p.n;
+            const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                    static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+            for (int chunk = 0; chunk < kBN / 32; ++chunk) {
+                uint32_t v[32];
+                tmem_ld32(t_addr + chunk * 32, v);
+                tmem_ld_wait();
+                const int64_t j0 = static_cast<int64_t>(g.nb) * kBN + chunk * 32;
+                if (valid && j0 < p.n) {
+                    if (out_vec_ok && j0 + 32 <= p.n) {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + j0);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            __stcs(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                        __uint_as_float(v[4 * q + 2]),
+                                                        __uint_as_float(v[4 * q + 3])));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (j0 + c < p.n) orow[j0 + c] = __uint_as_float(v[c]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    } else {
+        // ---------------- activation producers (warps 6..9) ----------------
+        const int tid = threadIdx.x - kProducerWarp0 * 32;  // 0..127
+        const int sub = tid & 7;       // 16-byte chunk (8 elements) of the 64-wide k-block
+        const int rsub = tid >> 3;     // rows rsub, rsub + 16, ...
+        const uint64_t pol = policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
+            const float *src[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int i = rsub + 16 * q;
+                src[q] = nullptr;
+                if (i < g.rows) {
+                    const uint32_t r = p.routed_rows[static_cast<int64_t>(g.e) * m + g.mb * kBM + i];
+                    const int64_t tok = r / p.top_k, slot = r % p.top_k;
+                    src[q] = p.x + tok * p.x_token_stride + slot * p.x_slot_stride;
+                }
+            }
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                int ready = 0;
+                if (lane == 0) ready = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (!ready) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_device_error(p.err, kKidGroupedTc);
+                    }
+                    ok = false;
+                    break;
+                }
+                const int64_t k0 = static_cast<int64_t>(kb) * kBK + sub * 8;
+                float4 a[8][2];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (src[q] != nullptr && k0 < p.k) {
+                        a[q][0] = ld_f4_policy(src[q] + k0, pol);
+                        a[q][1] = ld_f4_policy(src[q] + k0 + 4, pol);
+                    } else {
+                        a[q][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        a[q][1] = a[q][0];
+                    }
+                }
+                const uint32_t s_hi = s_base + stage * kStageBytes;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int i = rsub + 16 * q;
+                    const float f[8] = {a[q][0].x, a[q][0].y, a[q][0].z, a[q][0].w,
+                                        a[q][1].x, a[q][1].y, a[q][1].z, a[q][1].w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        hi[h] = pack_bf16(f[2 * h], f[2 * h + 1]);
+                        lo[h] = pack_bf16(f[2 * h] - bf16_lo_of(hi[h], 0),
+                                          f[2 * h + 1] - bf16_lo_of(hi[h], 1));
+                    }
+                    // 128-byte swizzle: 16-byte chunk c of row i sits at chunk c ^ (i % 8)
+                    const uint32_t off = static_cast<uint32_t>(i) * 128u +
+                                         (static_cast<uint32_t>(sub ^ (i & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + off),
+                                 "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + kXBytes + off),
+                                 "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                                 : "memory");
+                }
+                fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_bar(stage));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p,
+                                        int out_vec_ok, int num_sms, cudaStream_t s) {
+    static unsigned long long attr_set = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set |= bit;
+    }
+    grouped_tc_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(map_w, p, out_vec_ok);
+    return cudaGetLastError();
+}
+
+int grouped_tc_max_experts() { return kMaxExperts; }
+
+}  // namespace gbmm

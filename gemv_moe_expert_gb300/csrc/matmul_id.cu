@@ -42,10 +42,91 @@ __device__ __forceinline__ const float *x_row(const MatmulIdParams &p, uint32_t 
     return p.x + t * p.x_token_stride + s * p.x_slot_stride;
 }
 
+// One pass of a warp over its expert rows j (j0 + warp, step 8) for up to NR
+// routed rows (nr of them live) that selected the same expert.
+template <typename TW, int NR>
+__device__ __forceinline__ void direct_pass(const MatmulIdParams &p, const TW *W, const uint32_t *rows,
+                                            int nr, int64_t j0, int64_t j1, int warp, int lane,
+                                            int vec_ok) {
+    constexpr int V = Elem<TW>::kVec;
+    const float *xr[NR];
+    uint32_t orow[NR];
+#pragma unroll
+    for (int q = 0; q < NR; ++q) {
+        orow[q] = rows[q < nr ? q : 0];
+        xr[q] = x_row(p, orow[q]);
+    }
+    for (int64_t j = j0 + warp; j < j1; j += kDirectThreads / 32) {
+        const TW *wrow = W + j * p.k;
+        float acc[NR];
+#pragma unroll
+        for (int q = 0; q < NR; ++q) acc[q] = 0.f;
+        int64_t x_done = 0;
+        if (vec_ok) {
+            const int64_t nch = p.k / V;
+            int64_t c0 = 0;
+            for (; c0 + 32 * kDirectUnroll <= nch; c0 += 32 * kDirectUnroll) {
+                uint4 wv[kDirectUnroll];
+#pragma unroll
+                for (int u = 0; u < kDirectUnroll; ++u) wv[u] = ld_stream16(wrow + (c0 + u * 32 + lane) * V);
+#pragma unroll
+                for (int u = 0; u < kDirectUnroll; ++u) {
+                    float wf[V];
+                    unpack16<TW>(wv[u], wf);
+                    const int64_t xo = (c0 + u * 32 + lane) * V;
+#pragma unroll
+                    for (int q = 0; q < NR; ++q) {
+                        if (NR == 1 || q < nr) {
+#pragma unroll
+                            for (int h = 0; h < V / 4; ++h) {
+                                const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr[q] + xo) + h);
+                                acc[q] = fmaf(wf[4 * h + 0], xv.x, acc[q]);
+                                acc[q] = fmaf(wf[4 * h + 1], xv.y, acc[q]);
+                                acc[q] = fmaf(wf[4 * h + 2], xv.z, acc[q]);
+                                acc[q] = fmaf(wf[4 * h + 3], xv.w, acc[q]);
+                            }
+                        }
+                    }
+                }
+            }
+            for (int64_t c = c0 + lane; c < nch; c += 32) {
+                float wf[V];
+                unpack16<TW>(ld_stream16(wrow + c * V), wf);
+#pragma unroll
+                for (int q = 0; q < NR; ++q) {
+                    if (NR == 1 || q < nr) {
+#pragma unroll
+                        for (int h = 0; h < V / 4; ++h) {
+                            const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr[q] + c * V) + h);
+                            acc[q] = fmaf(wf[4 * h + 0], xv.x, acc[q]);
+                            acc[q] = fmaf(wf[4 * h + 1], xv.y, acc[q]);
+                            acc[q] = fmaf(wf[4 * h + 2], xv.z, acc[q]);
+                            acc[q] = fmaf(wf[4 * h + 3], xv.w, acc[q]);
+                        }
+                    }
+                }
+            }
+            x_done = nch * V;
+        }
+        for (int64_t x = x_done + lane; x < p.k; x += 32) {
+            const float wv = Elem<TW>::to_f(wrow[x]);
+#pragma unroll
+            for (int q = 0; q < NR; ++q)
+                if (NR == 1 || q < nr) acc[q] = fmaf(wv, xr[q][x], acc[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < NR; ++q) acc[q] = warp_sum(acc[q]);
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < NR; ++q)
+                if (NR == 1 || q < nr) p.out[static_cast<int64_t>(orow[q]) * p.n + j] = acc[q];
+        }
+    }
+}
+
 template <typename TW>
 __global__ void __launch_bounds__(kDirectThreads)
 matmul_id_direct_kernel(MatmulIdParams p, int vec_ok) {
-    constexpr int V = Elem<TW>::kVec;
     __shared__ uint32_t s_list[kDirectWindow];
     __shared__ int s_warp_cnt[kDirectThreads / 32];
 
@@ -83,80 +164,13 @@ matmul_id_direct_kernel(MatmulIdParams p, int vec_ok) {
             const TW *W = static_cast<const TW *>(p.w) + static_cast<int64_t>(e) * p.expert_stride_elems;
             for (int l0 = 0; l0 < total; l0 += kDirectXR) {
                 const int nr = total - l0 < kDirectXR ? total - l0 : kDirectXR;
-                const float *xr[kDirectXR];
-                uint32_t orow[kDirectXR];
-#pragma unroll
-                for (int q = 0; q < kDirectXR; ++q) {
-                    orow[q] = s_list[l0 + (q < nr ? q : 0)];
-                    xr[q] = x_row(p, orow[q]);
-                }
-                for (int64_t j = j0 + warp; j < j1; j += kDirectThreads / 32) {
-                    const TW *wrow = W + j * p.k;
-                    float acc[kDirectXR];
-#pragma unroll
-                    for (int q = 0; q < kDirectXR; ++q) acc[q] = 0.f;
-                    int64_t x_done = 0;
-                    if (vec_ok) {
-                        const int64_t nch = p.k / V;
-                        int64_t c0 = 0;
-                        for (; c0 + 32 * kDirectUnroll <= nch; c0 += 32 * kDirectUnroll) {
-                            uint4 wv[kDirectUnroll];
-#pragma unroll
-                            for (int u = 0; u < kDirectUnroll; ++u)
-                                wv[u] = ld_stream16(wrow + (c0 + u * 32 + lane) * V);
-#pragma unroll
-                            for (int u = 0; u < kDirectUnroll; ++u) {
-                                float wf[V];
-                                unpack16<TW>(wv[u], wf);
-                                const int64_t xo = (c0 + u * 32 + lane) * V;
-#pragma unroll
-                                for (int q = 0; q < kDirectXR; ++q) {
-                                    if (q < nr) {
-#pragma unroll
-                                        for (int h = 0; h < V / 4; ++h) {
-                                            const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr[q] + xo) + h);
-                                            acc[q] = fmaf(wf[4 * h + 0], xv.x, acc[q]);
-                                            acc[q] = fmaf(wf[4 * h + 1], xv.y, acc[q]);
-                                            acc[q] = fmaf(wf[4 * h + 2], xv.z, acc[q]);
-                                            acc[q] = fmaf(wf[4 * h + 3], xv.w, acc[q]);
-                                        }
-                                    }
-                                }
-                            }
-                        }
-                        for (int64_t c = c0 + lane; c < nch; c += 32) {
-                            float wf[V];
-                            unpack16<TW>(ld_stream16(wrow + c * V), wf);
-#pragma unroll
-                            for (int q = 0; q < kDirectXR; ++q) {
-                                if (q < nr) {
-#pragma unroll
-                                    for (int h = 0; h < V / 4; ++h) {
-                                        const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr[q] + c * V) + h);
-                                        acc[q] = fmaf(wf[4 * h + 0], xv.x, acc[q]);
-                                        acc[q] = fmaf(wf[4 * h + 1], xv.y, acc[q]);
-                                        acc[q] = fmaf(wf[4 * h + 2], xv.z, acc[q]);
-                                        acc[q] = fmaf(wf[4 * h + 3], xv.w, acc[q]);
-                                    }
-                                }
-                            }
-                        }
-                        x_done = nch * V;
-                    }
-                    for (int64_t x = x_done + lane; x < p.k; x += 32) {
-                        const float wv = Elem<TW>::to_f(wrow[x]);
-#pragma unroll
-                        for (int q = 0; q < kDirectXR; ++q)
-                            if (q < nr) acc[q] = fmaf(wv, xr[q][x], acc[q]);
-                    }
-#pragma unroll
-                    for (int q = 0; q < kDirectXR; ++q) acc[q] = warp_sum(acc[q]);
-                    if (lane == 0) {
-#pragma unroll
-                        for (int q = 0; q < kDirectXR; ++q)
-                            if (q < nr) p.out[static_cast<int64_t>(orow[q]) * p.n + j] = acc[q];
-                    }
-                }
+                // the common decode case is one routed row per expert: specialise
+                if (nr == 1)
+                    direct_pass<TW, 1>(p, W, s_list + l0, 1, j0, j1, warp, lane, vec_ok);
+                else if (nr == 2)
+                    direct_pass<TW, 2>(p, W, s_list + l0, 2, j0, j1, warp, lane, vec_ok);
+                else
+                    direct_pass<TW, kDirectXR>(p, W, s_list + l0, nr, j0, j1, warp, lane, vec_ok);
             }
             __syncthreads();  // s_list / s_warp_cnt are rewritten by the next (r, jt)
         }

@@ -139,6 +139,19 @@ def test_matmul_id_parity_small(oracle_mod, wdtype, route, layout):
     case = synth.matmul_id_case(f"{wdtype}-r{route}-l{layout}", wdtype, 150, 300, 520, 4, 12,
                                 route=route, input_layout=layout, stride_pad_elems=8, seed=3)
     Run(case).call().check(oracle_mod)
+    if route == 1:
+        want = "gbmm_matmul_id_grouped_tc" if wdtype == "bf16" else "gbmm_matmul_id_grouped_simt"
+        assert gb.gbmm_test_last_kernel() == want
+
+
+def test_grouped_tc_odd_shapes(oracle_mod):
+    # k not a multiple of 64, n not a multiple of 256 nor 4 (scalar epilogue stores),
+    # several row blocks for the largest experts, one expert with no rows
+    m, top_k, E = 700, 3, 7
+    ids = synth.distinct_ids(m, top_k, E - 1, seed=4)  # expert E-1 never selected
+    case = synth.matmul_id_case("odd", "bf16", m, 261, 200, top_k, E, route=1, ids=ids)
+    Run(case).call().check(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
 
 
 @pytest.mark.parametrize("route", [0, 1])
