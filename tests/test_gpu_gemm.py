@@ -89,7 +89,7 @@ def test_worked_examples(oracle_mod, dtype):
 
 TC_SHAPES = [
     (1, 128, 256, 64),        # exactly one tile, one k-block
-    (2, 200, 300, 150),       # ragged m, n and k tails, several tiles
+    (2, 200, 300, 152),       # ragged m, n and k tails, several tiles
     (1, 257, 513, 1000),      # one past the tile edges
     (3, 384, 256, 4096),      # long k
     (1, 1000, 40, 72),        # narrow n
