@@ -42,7 +42,12 @@ EXPORTS = (
     "gbmm_matmul_id", "gbmm_last_error", "gbmm_status_string", "gbmm_abi_version",
     "gbmm_device_error", "gbmm_test_inject_kernel_failure", "gbmm_test_launch_count",
     "gbmm_test_reset_launch_count", "gbmm_test_last_kernel", "gbmm_test_bounded_wait",
+    "gbmm_matmul_id_static_scratch",
 )
+
+# n_experts * m * 4 bytes of routed rows fit the fixed scratch of
+# gbmm_matmul_id_static_scratch
+STATIC_SCRATCH_ROUTED_ROWS_BYTES = 4 << 20
 
 
 class MatmulIdParams(ctypes.Structure):
@@ -123,6 +128,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gbmm_test_last_kernel.restype = ctypes.c_char_p
         lib.gbmm_test_bounded_wait.argtypes = [u64, vp, ctypes.POINTER(u32)]
         lib.gbmm_test_bounded_wait.restype = i32
+        lib.gbmm_matmul_id_static_scratch.argtypes = [ctypes.POINTER(MatmulIdParams), i32, vp, u64,
+                                                      vp, u64, vp, u64, vp, u64, vp,
+                                                      ctypes.POINTER(MatmulIdReceipt)]
+        lib.gbmm_matmul_id_static_scratch.restype = i32
         _lib = lib
         return lib
 
@@ -216,6 +225,18 @@ def gbmm_matmul_id(params: MatmulIdParams, weight_dtype, weights, weights_bytes,
                                _ptr(out), out_bytes,
                                ctypes.byref(scratch) if scratch is not None else None,
                                _stream(stream), ctypes.byref(rec))
+    return st, rec
+
+
+def gbmm_matmul_id_static_scratch(params: MatmulIdParams, weight_dtype, weights, weights_bytes,
+                                  input, input_bytes, ids, ids_bytes, out, out_bytes, stream=None):
+    """GroupedPrefill without caller scratch, for callers that cannot allocate
+    device memory (see include/gbmm.h).  Returns (status, MatmulIdReceipt)."""
+    rec = MatmulIdReceipt()
+    st = load().gbmm_matmul_id_static_scratch(ctypes.byref(params), _dt(weight_dtype),
+                                              _ptr(weights), weights_bytes, _ptr(input),
+                                              input_bytes, _ptr(ids), ids_bytes, _ptr(out),
+                                              out_bytes, _stream(stream), ctypes.byref(rec))
     return st, rec
 
 

@@ -406,6 +406,14 @@ Range range_of(const void *p, uint64_t bytes) {
 
 }  // namespace
 
+namespace gbmm {
+// Lets other translation units of the library set gbmm_last_error().
+int record_error(int status, const char *message) {
+    t_last_error = message ? message : "";
+    return status;
+}
+}  // namespace gbmm
+
 extern "C" {
 
 gbmm_status gbmm_gemm(gbmm_dtype dt, int64_t batch, int64_t m, int64_t n, int64_t k,

@@ -254,6 +254,50 @@ GBMM_API gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype w
                            const gbmm_matmul_id_scratch *scratch,
                            gbmm_stream stream, gbmm_matmul_id_receipt *receipt);
 
+/*
+ * gbmm_matmul_id_static_scratch -- the GroupedPrefill route of
+ * gbmm_matmul_id for callers that cannot allocate device memory.  (The
+ * pages have no counterpart: their grouped route always takes caller-owned
+ * scratch.)
+ *
+ * Who needs it: a caller that is handed only the operands and outputs of
+ * each call while someone else owns all other device memory (a plugin slot
+ * in another runtime), or a serving loop that may not call cudaMalloc once
+ * it runs, since an allocation can wait on a device-wide synchronisation.
+ * Such a caller cannot supply the expert_counts / routed_rows buffers.
+ *
+ * What it does: exactly gbmm_matmul_id with route GroupedPrefill (same
+ * arguments minus `scratch`, same results, two launches), with the scratch
+ * taken from one fixed array compiled into the library.  The array holds
+ * GBMM_GROUPED_MAX_EXPERTS counts and GBMM_STATIC_SCRATCH_ROUTED_ROWS_BYTES
+ * of routed rows, i.e. n_experts * m <= 1,048,576; it is reserved on every
+ * GPU that loads the library until the process exits.  The call allocates
+ * nothing and calls no allocating routine.
+ *
+ * Errors: GBMM_ERR_INVALID_ARGUMENT for a NULL params or a route other than
+ * GroupedPrefill; GBMM_ERR_SCRATCH (nothing launched) when n_experts * m * 4
+ * exceeds the array; otherwise every rule and status of gbmm_matmul_id.
+ *
+ * Sharing: every call on every stream of a device uses the same array, and
+ * the array keeps the last call's contents.  Nothing in it needs to start at
+ * zero (each call rewrites what it reads).  Calls whose work overlaps on the
+ * GPU -- concurrent streams, or host threads without stream ordering between
+ * them -- race on the array and corrupt each other's results; order them.
+ *
+ * Set-up: the first call on each device (that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and caches it; make that
+ * first call before any stream capture on the device.
+ */
+#define GBMM_STATIC_SCRATCH_ROUTED_ROWS_BYTES (4u << 20)
+GBMM_API gbmm_status gbmm_matmul_id_static_scratch(const gbmm_matmul_id_params *p,
+                                                   gbmm_dtype weight_dtype,
+                                                   const void *weights, uint64_t weights_bytes,
+                                                   const float *input, uint64_t input_bytes,
+                                                   const uint32_t *ids, uint64_t ids_bytes,
+                                                   float *out, uint64_t out_bytes,
+                                                   gbmm_stream stream,
+                                                   gbmm_matmul_id_receipt *receipt);
+
 /* ------------------------------------------------------------------------ */
 /* Errors, diagnostics                                                        */
 /* ------------------------------------------------------------------------ */
