@@ -319,6 +319,9 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
     p.sc = sc;
     p.ta = ta;
     p.tb = tb;
+    // a few thousand outputs: latency-bound, one output per thread
+    if (batch * m * n <= 16384 && k <= 4096)
+        return after_launch(launch_gemm_small(dt, p, stream), "gbmm_gemm_small", stream);
     return after_launch(launch_gemm_simt(dt, p, stream), "gbmm_gemm_simt", stream);
 }
 
@@ -568,13 +571,14 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
               p->n_experts <= static_cast<uint32_t>(grouped_tc_max_experts());
     if (tc) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-        cuuint64_t dims[3] = {p->k, p->n, p->n_experts};
-        cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->k) * 2, p->expert_stride_bytes};
-        cuuint32_t box[3] = {64u, 256u, 1u};
+        // weights: (k, n, expert), 256 x 64 boxes, 128-byte swizzle
+        cuuint64_t wdims[3] = {p->k, p->n, p->n_experts};
+        cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(p->k) * 2, p->expert_stride_bytes};
+        cuuint32_t wbox[3] = {static_cast<cuuint32_t>(grouped_tc_block_k()), 256u, 1u};
         cuuint32_t estr[3] = {1u, 1u, 1u};
         tc = enc != nullptr &&
-             enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), wdims, wstrides,
+                 wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
     if (tc) {

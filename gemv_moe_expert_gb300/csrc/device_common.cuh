@@ -188,6 +188,38 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Gather four rows (row coordinates y0..y3, each box one row high) of a 2-D
+// tensor at column c0 into consecutive shared memory.
+__device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t c0, int32_t y0, int32_t y1, int32_t y2,
+                                                 int32_t y3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "l"(policy)
+        : "memory");
+}
+
+// Prefetch into L2 only (no shared-memory destination, no completion):
+// four gathered rows of a 2-D tensor / one tile of a 3-D tensor.
+__device__ __forceinline__ void tma_prefetch_gather4(const CUtensorMap *map, int32_t c0, int32_t y0,
+                                                     int32_t y1, int32_t y2, int32_t y3) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile::gather4 [%0, {%1, %2, %3, %4, %5}];" ::"l"(map),
+        "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+// Bring the 128-byte line holding p into L2, marked evict-last.
+__device__ __forceinline__ void prefetch_l2_evict_last(const void *p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 // L2 cache policies: data read once (streamed) / data re-read by many CTAs.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -266,6 +298,18 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Same for 64-byte swizzling: rows of 64 bytes (32 16-bit elements), 8-row
+// groups 512 bytes apart, swizzle mode 4 = 64B.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(512u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(4u) << 61;
     return d;
 }
 

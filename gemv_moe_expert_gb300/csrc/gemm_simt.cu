@@ -100,6 +100,74 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmParams p) {
     }
 }
 
+// Small problems are latency-bound.  A CTA owns 16 x 16 outputs; per chunk of
+// 128 along k it first issues every load of its A rows and B columns at once
+// (one memory round trip), stages them in shared memory as f32, then each
+// thread computes one output.  For k <= 128 the whole problem costs one round
+// trip plus the launch.
+constexpr int kSmallT = 16;
+constexpr int kSmallK = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(256) gemm_small_kernel(GemmParams p) {
+    __shared__ float As[kSmallT][kSmallK + 1];
+    __shared__ float Bs[kSmallK][kSmallT + 1];
+    const int tj = threadIdx.x & 15, ti = threadIdx.x >> 4;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.y) * kSmallT;
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kSmallT;
+    for (int64_t bat = blockIdx.z; bat < p.batch; bat += gridDim.z) {
+        const T *A = static_cast<const T *>(p.a) + bat * p.sa;
+        const T *B = static_cast<const T *>(p.b) + bat * p.sb;
+        float acc = 0.f;
+        for (int64_t k0 = 0; k0 < p.k; k0 += kSmallK) {
+            // 16 x 128 of op(A) and 128 x 16 of op(B): 8 + 8 independent loads per thread,
+            // ordered along each operand's contiguous dimension
+            float av[8], bv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = threadIdx.x + 256 * u;  // 0..2047
+                int r, x;
+                if (p.ta) { r = idx % kSmallT; x = idx / kSmallT; } else { x = idx % kSmallK; r = idx / kSmallK; }
+                const int64_t gi = i0 + r, gx = k0 + x;
+                av[u] = (gi < p.m && gx < p.k) ? Elem<T>::to_f(A[p.ta ? gx * p.lda + gi : gi * p.lda + gx]) : 0.f;
+                int c, y;
+                if (p.tb) { y = idx % kSmallK; c = idx / kSmallK; } else { c = idx % kSmallT; y = idx / kSmallT; }
+                const int64_t gj = j0 + c, gy = k0 + y;
+                bv[u] = (gj < p.n && gy < p.k) ? Elem<T>::to_f(B[p.tb ? gj * p.ldb + gy : gy * p.ldb + gj]) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = threadIdx.x + 256 * u;
+                if (p.ta) As[idx % kSmallT][idx / kSmallT] = av[u]; else As[idx / kSmallK][idx % kSmallK] = av[u];
+                if (p.tb) Bs[idx % kSmallK][idx / kSmallK] = bv[u]; else Bs[idx / kSmallT][idx % kSmallT] = bv[u];
+            }
+            __syncthreads();
+            const int64_t kn = p.k - k0 < kSmallK ? p.k - k0 : kSmallK;
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+            int x = 0;
+            for (; x + 4 <= kn; x += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) part[u] = fmaf(As[ti][x + u], Bs[x + u][tj], part[u]);
+            }
+            for (; x < kn; ++x) part[0] = fmaf(As[ti][x], Bs[x][tj], part[0]);
+            acc += (part[0] + part[1]) + (part[2] + part[3]);
+            __syncthreads();
+        }
+        const int64_t gi = i0 + ti, gj = j0 + tj;
+        if (gi < p.m && gj < p.n)
+            static_cast<T *>(p.c)[bat * p.sc + gi * p.ldc + gj] = Elem<T>::from_f(acc);
+    }
+}
+
+template <typename T>
+cudaError_t small_t(const GemmParams &p, cudaStream_t s) {
+    const int64_t gx = (p.n + 15) / 16, gy = (p.m + 15) / 16;
+    if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
+    const unsigned gz = static_cast<unsigned>(p.batch < 65535 ? p.batch : 65535);
+    gemm_small_kernel<T><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), gz), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t simt_t(const GemmParams &p, cudaStream_t s) {
     const int64_t gx = (p.n + kBN - 1) / kBN;
@@ -111,6 +179,15 @@ cudaError_t simt_t(const GemmParams &p, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_small(int dt, const GemmParams &p, cudaStream_t s) {
+    switch (dt) {
+    case kF32: return small_t<float>(p, s);
+    case kF16: return small_t<__half>(p, s);
+    case kBF16: return small_t<__nv_bfloat16>(p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s) {
     switch (dt) {

@@ -55,39 +55,32 @@ gemv_rowdot_kernel(GemvParams p) {
             const T *mrow = mat + row * p.mat_rs;
 
             if (p.vec_ok) {
+                // groups of kU 16-byte vectors per lane, all loads of a group issued
+                // before any use (the last group is predicated, not split off)
+                constexpr int kU = NV <= 2 ? 2 * kRowdotUnroll : kRowdotUnroll;
                 const int64_t nch = p.k / V;
-                int64_t c0 = 0;
-                for (; c0 + 32 * kRowdotUnroll <= nch; c0 += 32 * kRowdotUnroll) {
-                    uint4 w[kRowdotUnroll];
+                for (int64_t c0 = 0; c0 < nch; c0 += 32 * kU) {
+                    uint4 w[kU];
 #pragma unroll
-                    for (int u = 0; u < kRowdotUnroll; ++u)
-                        w[u] = ld_stream16(mrow + (c0 + u * 32 + lane) * V);
-#pragma unroll
-                    for (int u = 0; u < kRowdotUnroll; ++u) {
-                        float wf[V];
-                        unpack16<T>(w[u], wf);
-                        const int64_t off = (c0 + u * 32 + lane) * V;
-#pragma unroll
-                        for (int r = 0; r < NV; ++r) {
-                            if (r < nvec) {
-                                float xf[V];
-                                unpack16<T>(ld_cached16(vec + r * p.vec_rr + off), xf);
-#pragma unroll
-                                for (int i = 0; i < V; ++i) acc[r] = fmaf(wf[i], xf[i], acc[r]);
-                            }
-                        }
+                    for (int u = 0; u < kU; ++u) {
+                        const int64_t c = c0 + u * 32 + lane;
+                        w[u] = c < nch ? ld_stream16(mrow + c * V) : make_uint4(0u, 0u, 0u, 0u);
                     }
-                }
-                for (int64_t c = c0 + lane; c < nch; c += 32) {
-                    float wf[V];
-                    unpack16<T>(ld_stream16(mrow + c * V), wf);
 #pragma unroll
-                    for (int r = 0; r < NV; ++r) {
-                        if (r < nvec) {
-                            float xf[V];
-                            unpack16<T>(ld_cached16(vec + r * p.vec_rr + c * V), xf);
+                    for (int u = 0; u < kU; ++u) {
+                        const int64_t c = c0 + u * 32 + lane;
+                        if (c < nch) {
+                            float wf[V];
+                            unpack16<T>(w[u], wf);
 #pragma unroll
-                            for (int i = 0; i < V; ++i) acc[r] = fmaf(wf[i], xf[i], acc[r]);
+                            for (int r = 0; r < NV; ++r) {
+                                if (r < nvec) {
+                                    float xf[V];
+                                    unpack16<T>(ld_cached16(vec + r * p.vec_rr + c * V), xf);
+#pragma unroll
+                                    for (int i = 0; i < V; ++i) acc[r] = fmaf(wf[i], xf[i], acc[r]);
+                                }
+                            }
                         }
                     }
                 }

@@ -8,25 +8,32 @@
 // For expert e and its routed rows r_0 < r_1 < ... (routed_rows[e*m + i],
 // i < expert_counts[e]) the kernel computes the GEMM
 //     out[r_i, j] = sum_x W_e[j, x] * xrow(r_i)[x]
-// with M = routed rows (gathered), N = n, K = k, in tiles of 128 rows x 256
+// with M = routed rows (gathered), N = n, K = k, in tiles of 128 rows x 512
 // outputs.  The activations are f32; tensor cores take bf16 pairs, so every
 // activation is split exactly as x = hi + lo with hi = bf16(x) and
 // lo = bf16(x - hi) and both halves are multiplied by the same bf16 weight
-// tile into one f32 accumulator.  The split leaves a relative error of at
+// tiles into one f32 accumulator.  The split leaves a relative error of at
 // most 2^-16 on each activation (against 2^-8 for a single bf16 rounding),
 // so the result stays an f32-accurate expert product.
 //
-// One persistent CTA per SM, 10 warps:
-//   warp 0     TMA: 256x64 bf16 weight tiles of W_e (3-D tensor map over
-//              (k, n, expert), 128-byte swizzle), streamed with L2 evict-first
-//   warp 1     TMEM allocation (two 128x256 f32 accumulators) and the MMA
-//              issuer: 8 x tcgen05.mma (M=128, N=256, K=16) per 64-wide k-block
+// The costly operand is the activation tile: its rows are gathered, and each
+// gathered row must be split into hi / lo on the SMs.  A tile 512 outputs
+// wide (two 128x256 f32 accumulators, the whole tensor memory) amortises one
+// gather + split over twice the weight columns of a 256-wide tile.
+//
+// One persistent CTA per SM, 14 warps:
+//   warp 0     TMA: two 256x64 bf16 weight tiles of W_e per k-block (3-D
+//              tensor map over (k, n, expert), 128-byte swizzle, L2
+//              evict-first), with L2 prefetches issued a few k-blocks ahead
+//   warp 1     TMEM allocation (512 columns) and the MMA issuer:
+//              16 x tcgen05.mma (M=128, N=256, K=16) per 64-wide k-block
 //   warps 2..5 epilogue: TMEM -> registers -> f32 rows of `out`, scattered to
 //              their routed rows (each thread writes 128 contiguous bytes)
-//   warps 6..9 activation producers: gather 128 routed x rows (f32, L2
-//              evict-last: each token row serves top_k experts), split into
-//              bf16 hi/lo, write the 128-byte-swizzled K-major smem layout the
-//              MMA descriptors expect, then arrive on the stage barrier.
+//   warps 6..13 activation producers: gather the 128 routed x rows (f32, L2
+//              evict-last: each token row serves top_k experts) two k-blocks
+//              ahead of use, split into bf16 hi / lo, write the 128-byte-
+//              swizzled K-major smem layout the MMA descriptors expect.
+// Shared memory: 2 stages x (x_hi 16 KB + x_lo 16 KB + 2 weight tiles 64 KB).
 // Tile list: every CTA derives it from expert_counts (written by the map
 // launch before this one): tiles ordered by expert, then row block, then
 // output block.  Every mbarrier wait is bounded; see gemm_tc.cu.
@@ -37,14 +44,18 @@ namespace gbmm {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBNH = 256;          // one accumulator / one MMA N
+constexpr int kBN = 2 * kBNH;      // tile width
 constexpr int kBK = 64;
-constexpr int kStages = 3;
-constexpr int kThreads = 320;
+constexpr int kStages = 2;
+constexpr int kThreads = 448;
+constexpr int kRowsPerProducer = 4;  // 8 producer warps x 32 row groups x 4 = 128 rows
 constexpr int kProducerWarp0 = 6;
-constexpr uint32_t kXBytes = kBM * kBK * 2;  // one bf16 half of the activation tile
-constexpr uint32_t kWBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = 2 * kXBytes + kWBytes;
+constexpr int kWPrefetch = 4;      // k-blocks of weight L2 prefetch ahead
+constexpr int kXPrefetch = 4;      // k-blocks of activation L2 prefetch ahead of the loads
+constexpr uint32_t kXBytes = kBM * kBK * 2;   // one bf16 half of the activation tile
+constexpr uint32_t kWBytes = kBNH * kBK * 2;  // one weight tile
+constexpr uint32_t kStageBytes = 2 * kXBytes + 2 * kWBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + (kMaxExperts + 8) * 4 + 256 + 1024;
@@ -76,8 +87,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ float bf16_lo_of(uint32_t packed, int half) {
+__device__ __forceinline__ float bf16_half(uint32_t packed, int half) {
     return __uint_as_float(half ? (packed & 0xffff0000u) : (packed << 16));
+}
+
+// one lane waits, the warp follows its verdict (keeps the warp converged)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
+                                          volatile int *abort_flag, int lane) {
+    int ready = 0;
+    if (lane == 0) ready = mbar_wait_bounded(bar, parity, limit, abort_flag);
+    ready = __shfl_sync(0xffffffffu, ready, 0);
+    __syncwarp();
+    return ready != 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -87,16 +108,16 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     const uint32_t s_base = raw_addr + pad;
-    // stage s: x_hi at s_base + s*kStageBytes, x_lo after it, then the weight tile
+    // stage s at s_base + s*kStageBytes: x_hi, x_lo, weight tile 0, weight tile 1
     uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(prefix + kMaxExperts + 8);
     const uint32_t bar0 = smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    const uint32_t tfull_bar = bar0 + 8u * (2 * kStages);
+    const uint32_t tempty_bar = bar0 + 8u * (2 * kStages + 1);
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ uint32_t warp_tot[kThreads / 32];
 
@@ -105,16 +126,15 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     const int E = static_cast<int>(p.n_experts);
     const int m = static_cast<int>(p.m);
     const int nblk = static_cast<int>((p.n + kBN - 1) / kBN);
+    const uint64_t lim = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1 + 4);  // TMA arrive + one arrive per producer warp
-            mbar_init(empty_bar(s), 1);
+            mbar_init(full_bar(s), 1 + 8);  // TMA thread's arrive + one arrive per producer warp
+            mbar_init(empty_bar(s), 1);     // MMA commit
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
-        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, 4);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -127,7 +147,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 
     // tile prefix over experts: prefix[e] = sum_{e' < e} ceil(count/128) * nblk
     {
-        constexpr int kPer = 4;  // 320 threads x 4 >= 1024 + 1 entries
+        constexpr int kPer = 3;  // 448 threads x 3 >= 1024 + 1 entries
         uint32_t v[kPer];
         uint32_t sum = 0;
 #pragma unroll
@@ -151,7 +171,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         __syncthreads();
         uint32_t base = 0;
         for (int w = 0; w < warp; ++w) base += warp_tot[w];
-        uint32_t run = base + incl - sum;  // exclusive prefix of this thread's first entry
+        uint32_t run = base + incl - sum;
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
             const int e = threadIdx.x * kPer + q;
@@ -175,14 +195,24 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
+                const int n0 = g.nb * kBN;
+                for (int kb = 0; kb < kWPrefetch && kb < kblocks; ++kb) {
+                    tma_prefetch_3d(&map_w, kb * kBK, n0, g.e);
+                    tma_prefetch_3d(&map_w, kb * kBK, n0 + kBNH, g.e);
+                }
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                    if (kb + kWPrefetch < kblocks) {
+                        tma_prefetch_3d(&map_w, (kb + kWPrefetch) * kBK, n0, g.e);
+                        tma_prefetch_3d(&map_w, (kb + kWPrefetch) * kBK, n0 + kBNH, g.e);
+                    }
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, lim, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage), kWBytes);
-                    tma_load_3d_hint(s_base + stage * kStageBytes + 2 * kXBytes, &map_w, full_bar(stage),
-                                     kb * kBK, g.nb * kBN, g.e, pol);
+                    const uint32_t s_w = s_base + stage * kStageBytes + 2 * kXBytes;
+                    mbar_arrive_expect_tx(full_bar(stage), 2 * kWBytes);
+                    tma_load_3d_hint(s_w, &map_w, full_bar(stage), kb * kBK, n0, g.e, pol);
+                    tma_load_3d_hint(s_w + kWBytes, &map_w, full_bar(stage), kb * kBK, n0 + kBNH, g.e, pol);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -193,45 +223,50 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             if (!ok) {
                 *abort_flag = 1;
                 report_device_error(p.err, kKidGroupedTc);
-                // the stage barriers also count producer-warp arrivals, so wait on
-                // the bytes only: each issued copy completes its own transaction
+                // the stage barriers also count producer-warp arrivals, so a stage
+                // whose copies landed may still read as incomplete: the bounded
+                // wait below then just runs out (the copies are long done)
                 for (int s = 0; s < kStages; ++s) {
                     const uint32_t n_s = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
-                    if (n_s > 0) mbar_wait_bounded(full_bar(s), (n_s - 1u) & 1u, p.wait_limit_ns, nullptr);
+                    if (n_s > 0) mbar_wait_bounded(full_bar(s), (n_s - 1u) & 1u, lim, nullptr);
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t kIdesc = idesc_f16(1u, kBM, kBN);  // bf16 x bf16 -> f32
+            constexpr uint32_t kIdesc = idesc_f16(1u, kBM, kBNH);  // bf16 x bf16 -> f32
             int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
+            uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+                // both accumulators drained by the epilogue of the previous tile
+                if (!mbar_wait_bounded(tempty_bar, acc_phase ^ 1u, lim, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag)) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, lim, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t s_hi = s_base + stage * kStageBytes;
                     const uint32_t s_lo = s_hi + kXBytes;
-                    const uint32_t s_w = s_hi + 2 * kXBytes;
+                    const uint32_t s_w0 = s_hi + 2 * kXBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t dw = sdesc_kmajor_sw128(s_w + kk * 32);
-                        umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_hi + kk * 32), dw, kIdesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
-                        umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_lo + kk * 32), dw, kIdesc, 1u);
+                        const uint64_t da_hi = sdesc_kmajor_sw128(s_hi + kk * 32);
+                        const uint64_t da_lo = sdesc_kmajor_sw128(s_lo + kk * 32);
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t dw = sdesc_kmajor_sw128(s_w0 + h * kWBytes + kk * 32);
+                            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * kBNH);
+                            umma_f16_ss(d_tmem, da_hi, dw, kIdesc, acc);
+                            umma_f16_ss(d_tmem, da_lo, dw, kIdesc, 1u);
+                        }
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == kStages) {
@@ -240,35 +275,29 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(acc));
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                umma_commit(tfull_bar);
+                acc_phase ^= 1u;
             }
             if (!ok) {
                 *abort_flag = 1;
                 report_device_error(p.err, kKidGroupedTc);
             }
             umma_commit(drain_bar);
-            mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, nullptr);
+            mbar_wait_bounded(drain_bar, 0, lim, nullptr);
         }
     } else if (warp < kProducerWarp0) {
         // ---------------- epilogue (warps 2..5) ----------------
         const int quarter = warp & 3;
-        int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
-            int ready = 0;
-            if (lane == 0) ready = mbar_wait_bounded(tfull_bar(acc), acc_phase, p.wait_limit_ns, abort_flag);
-            ready = __shfl_sync(0xffffffffu, ready, 0);
-            if (!ready) {
+            if (!warp_wait(tfull_bar, acc_phase, lim, abort_flag, lane)) {
                 if (lane == 0) {
                     *abort_flag = 1;
                     report_device_error(p.err, kKidGroupedTc);
                 }
                 break;
             }
-            __syncwarp();
             tc_fence_after();
             const int i = quarter * 32 + lane;
             const bool valid = i < g.rows;
@@ -276,8 +305,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                                                                          g.mb * kBM + i])
                                     : 0;
             float *orow = p.out + r * p.n;
-            const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                    static_cast<uint32_t>(acc * kBN);
+            const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
             for (int chunk = 0; chunk < kBN / 32; ++chunk) {
                 uint32_t v[32];
@@ -301,74 +329,83 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            if (lane == 0) mbar_arrive(tempty_bar);
+            acc_phase ^= 1u;
         }
     } else {
-        // ---------------- activation producers (warps 6..9) ----------------
-        const int tid = threadIdx.x - kProducerWarp0 * 32;  // 0..127
-        const int sub = tid & 7;       // 16-byte chunk (8 elements) of the 64-wide k-block
-        const int rsub = tid >> 3;     // rows rsub, rsub + 16, ...
+        // ---------------- activation producers (warps 6..13) ----------------
+        // Each thread owns one 16-byte chunk (8 elements) of the 64-wide k-block
+        // in 4 rows.  Loads run two k-blocks ahead of the conversion, in a
+        // ring of registers, so gathered rows stream in while earlier stages
+        // are converted and while the tensor cores are busy.
+        const int tid = threadIdx.x - kProducerWarp0 * 32;  // 0..255
+        const int sub = tid & 7;
+        const int rsub = tid >> 3;  // rows rsub + 32 q, q < 4
         const uint64_t pol = policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
-            const float *src[8];
+            const float *src[kRowsPerProducer];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int i = rsub + 16 * q;
+            for (int q = 0; q < kRowsPerProducer; ++q) {
+                const int i = rsub + 32 * q;
                 src[q] = nullptr;
                 if (i < g.rows) {
                     const uint32_t r = p.routed_rows[static_cast<int64_t>(g.e) * m + g.mb * kBM + i];
                     const int64_t tok = r / p.top_k, slot = r % p.top_k;
-                    src[q] = p.x + tok * p.x_token_stride + slot * p.x_slot_stride;
+                    src[q] = p.x + tok * p.x_token_stride + slot * p.x_slot_stride + sub * 8;
                 }
             }
-            bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                int ready = 0;
-                if (lane == 0) ready = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag);
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (!ready) {
+            float4 ring0[kRowsPerProducer][2], ring1[kRowsPerProducer][2], ring2[kRowsPerProducer][2];
+            auto issue = [&](float4 (&buf)[kRowsPerProducer][2], int kb) {
+                // L2 prefetch of the rows' segment kXPrefetch k-blocks further on:
+                // one thread per 128-byte line (chunks 0 and 4 of the 256-byte segment)
+                if ((sub & 3) == 0 && kb + kXPrefetch < kblocks &&
+                    static_cast<int64_t>(kb + kXPrefetch) * kBK + sub * 8 < p.k) {
+#pragma unroll
+                    for (int q = 0; q < kRowsPerProducer; ++q)
+                        if (src[q] != nullptr)
+                            prefetch_l2_evict_last(src[q] + static_cast<int64_t>(kb + kXPrefetch) * kBK);
+                }
+                const bool in_k = kb < kblocks && static_cast<int64_t>(kb) * kBK + sub * 8 < p.k;
+#pragma unroll
+                for (int q = 0; q < kRowsPerProducer; ++q) {
+                    if (in_k && src[q] != nullptr) {
+                        buf[q][0] = ld_f4_policy(src[q] + static_cast<int64_t>(kb) * kBK, pol);
+                        buf[q][1] = ld_f4_policy(src[q] + static_cast<int64_t>(kb) * kBK + 4, pol);
+                    } else {
+                        buf[q][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        buf[q][1] = buf[q][0];
+                    }
+                }
+            };
+            auto consume = [&](float4 (&buf)[kRowsPerProducer][2]) -> bool {
+                if (!warp_wait(empty_bar(stage), phase ^ 1u, lim, abort_flag, lane)) {
                     if (lane == 0) {
                         *abort_flag = 1;
                         report_device_error(p.err, kKidGroupedTc);
                     }
-                    ok = false;
-                    break;
-                }
-                const int64_t k0 = static_cast<int64_t>(kb) * kBK + sub * 8;
-                float4 a[8][2];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (src[q] != nullptr && k0 < p.k) {
-                        a[q][0] = ld_f4_policy(src[q] + k0, pol);
-                        a[q][1] = ld_f4_policy(src[q] + k0 + 4, pol);
-                    } else {
-                        a[q][0] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        a[q][1] = a[q][0];
-                    }
+                    return false;
                 }
                 const uint32_t s_hi = s_base + stage * kStageBytes;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int i = rsub + 16 * q;
-                    const float f[8] = {a[q][0].x, a[q][0].y, a[q][0].z, a[q][0].w,
-                                        a[q][1].x, a[q][1].y, a[q][1].z, a[q][1].w};
+                for (int q = 0; q < kRowsPerProducer; ++q) {
+                    const int i = rsub + 32 * q;
+                    const float f[8] = {buf[q][0].x, buf[q][0].y, buf[q][0].z, buf[q][0].w,
+                                        buf[q][1].x, buf[q][1].y, buf[q][1].z, buf[q][1].w};
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         hi[h] = pack_bf16(f[2 * h], f[2 * h + 1]);
-                        lo[h] = pack_bf16(f[2 * h] - bf16_lo_of(hi[h], 0),
-                                          f[2 * h + 1] - bf16_lo_of(hi[h], 1));
+                        lo[h] = pack_bf16(f[2 * h] - bf16_half(hi[h], 0), f[2 * h + 1] - bf16_half(hi[h], 1));
                     }
                     // 128-byte swizzle: 16-byte chunk c of row i sits at chunk c ^ (i % 8)
                     const uint32_t off = static_cast<uint32_t>(i) * 128u +
                                          (static_cast<uint32_t>(sub ^ (i & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + off),
-                                 "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + off), "r"(hi[0]),
+                                 "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
                                  : "memory");
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + kXBytes + off),
                                  "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
@@ -381,8 +418,20 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     stage = 0;
                     phase ^= 1u;
                 }
+                return true;
+            };
+            issue(ring0, 0);
+            issue(ring1, 1);
+            for (int kb = 0; kb < kblocks && ok; kb += 3) {
+                issue(ring2, kb + 2);
+                ok = consume(ring0);
+                if (!ok || kb + 1 >= kblocks) break;
+                issue(ring0, kb + 3);
+                ok = consume(ring1);
+                if (!ok || kb + 2 >= kblocks) break;
+                issue(ring1, kb + 4);
+                ok = consume(ring2);
             }
-            if (!ok) break;
         }
     }
 
@@ -396,8 +445,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 
 }  // namespace
 
-cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p,
-                                        int out_vec_ok, int num_sms, cudaStream_t s) {
+cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
+                                        int num_sms, cudaStream_t s) {
     static unsigned long long attr_set = 0;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -413,5 +462,6 @@ cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulId
 }
 
 int grouped_tc_max_experts() { return kMaxExperts; }
+int grouped_tc_block_k() { return kBK; }
 
 }  // namespace gbmm

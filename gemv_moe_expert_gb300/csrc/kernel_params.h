@@ -93,15 +93,17 @@ cudaError_t launch_fill_zero(int dt, void *c, int64_t batch, int64_t m, int64_t 
 cudaError_t launch_gemv_rowdot(int dt, const GemvParams &p, cudaStream_t s);
 cudaError_t launch_gemv_coldot(int dt, const GemvParams &p, cudaStream_t s);
 cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s);
+cudaError_t launch_gemm_small(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                            const GemmTcParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s);
-cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p,
-                                        int out_vec_ok, int num_sms, cudaStream_t s);
+cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
+                                        int num_sms, cudaStream_t s);
 cudaError_t launch_bounded_wait_test(uint32_t *err, uint64_t limit_ns, cudaStream_t s);
 int grouped_tc_max_experts();
+int grouped_tc_block_k();
 
 int gemm_tc_block_m();
 int gemm_tc_block_n();

@@ -17,14 +17,20 @@
 // the number of tokens that picked it.  Rows of W are read as coalesced
 // 16-byte vectors (L1 bypassed), activations through L1.
 //
-// Routing map.  One CTA of 32 warps builds expert_counts and routed_rows
-// without atomics: each warp owns a contiguous segment of routed rows,
-// counts it per expert with __match_any_sync (one leader lane per distinct
-// id updates the warp's private counter row in shared memory), the per
-// expert counts are scanned across warps in row order, and a second pass
+// Routing map.  One cluster of 8 CTAs x 32 warps builds expert_counts and
+// routed_rows without atomics: each warp owns a contiguous segment of routed
+// rows and counts it per expert (lanes holding the same id are found with
+// one warp ballot per id bit; one leader lane per distinct id updates the
+// warp's private counter row in shared memory), the per
+// expert counts are scanned across warps and, through distributed shared
+// memory, across the cluster's CTAs in row order, and a second pass
 // scatters every row index to its final, ascending position.  Extra CTAs of
 // the same launch zero-fill output rows whose id is out of range.
+#include <cooperative_groups.h>
+
 #include "device_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace gbmm {
 
@@ -124,6 +130,65 @@ __device__ __forceinline__ void direct_pass(const MatmulIdParams &p, const TW *W
     }
 }
 
+// The decode case: one routed row per expert.  A warp streams two expert rows
+// (j and j + 8) at once, so twice the 16-byte loads are in flight per lane.
+template <typename TW>
+__device__ __forceinline__ void direct_pass_single(const MatmulIdParams &p, const TW *W, uint32_t orow,
+                                                   int64_t j0, int64_t j1, int warp, int lane) {
+    constexpr int V = Elem<TW>::kVec;
+    const float *xr = x_row(p, orow);
+    const int64_t nch = p.k / V;
+    constexpr int kStep = kDirectThreads / 32;
+    for (int64_t ja = j0 + warp; ja < j1; ja += 2 * kStep) {
+        const int64_t jb = ja + kStep;
+        const bool has_b = jb < j1;
+        const TW *wa = W + ja * p.k;
+        const TW *wb = W + (has_b ? jb : ja) * p.k;
+        float acc_a = 0.f, acc_b = 0.f;
+        for (int64_t c0 = 0; c0 < nch; c0 += 32 * kDirectUnroll) {
+            uint4 va[kDirectUnroll], vb[kDirectUnroll];
+#pragma unroll
+            for (int u = 0; u < kDirectUnroll; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                const bool in = c < nch;
+                va[u] = in ? ld_stream16(wa + c * V) : make_uint4(0u, 0u, 0u, 0u);
+                vb[u] = in && has_b ? ld_stream16(wb + c * V) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < kDirectUnroll; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                if (c < nch) {
+                    float fa[V], fb[V];
+                    unpack16<TW>(va[u], fa);
+                    unpack16<TW>(vb[u], fb);
+#pragma unroll
+                    for (int h = 0; h < V / 4; ++h) {
+                        const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr + c * V) + h);
+                        acc_a = fmaf(fa[4 * h + 0], xv.x, acc_a);
+                        acc_a = fmaf(fa[4 * h + 1], xv.y, acc_a);
+                        acc_a = fmaf(fa[4 * h + 2], xv.z, acc_a);
+                        acc_a = fmaf(fa[4 * h + 3], xv.w, acc_a);
+                        acc_b = fmaf(fb[4 * h + 0], xv.x, acc_b);
+                        acc_b = fmaf(fb[4 * h + 1], xv.y, acc_b);
+                        acc_b = fmaf(fb[4 * h + 2], xv.z, acc_b);
+                        acc_b = fmaf(fb[4 * h + 3], xv.w, acc_b);
+                    }
+                }
+            }
+        }
+        for (int64_t x = nch * V + lane; x < p.k; x += 32) {
+            acc_a = fmaf(Elem<TW>::to_f(wa[x]), xr[x], acc_a);
+            acc_b = fmaf(Elem<TW>::to_f(wb[x]), xr[x], acc_b);
+        }
+        acc_a = warp_sum(acc_a);
+        acc_b = warp_sum(acc_b);
+        if (lane == 0) {
+            p.out[static_cast<int64_t>(orow) * p.n + ja] = acc_a;
+            if (has_b) p.out[static_cast<int64_t>(orow) * p.n + jb] = acc_b;
+        }
+    }
+}
+
 template <typename TW>
 __global__ void __launch_bounds__(kDirectThreads)
 matmul_id_direct_kernel(MatmulIdParams p, int vec_ok) {
@@ -165,7 +230,9 @@ matmul_id_direct_kernel(MatmulIdParams p, int vec_ok) {
             for (int l0 = 0; l0 < total; l0 += kDirectXR) {
                 const int nr = total - l0 < kDirectXR ? total - l0 : kDirectXR;
                 // the common decode case is one routed row per expert: specialise
-                if (nr == 1)
+                if (nr == 1 && vec_ok)
+                    direct_pass_single<TW>(p, W, s_list[l0], j0, j1, warp, lane);
+                else if (nr == 1)
                     direct_pass<TW, 1>(p, W, s_list + l0, 1, j0, j1, warp, lane, vec_ok);
                 else if (nr == 2)
                     direct_pass<TW, 2>(p, W, s_list + l0, 2, j0, j1, warp, lane, vec_ok);
@@ -184,6 +251,19 @@ matmul_id_direct_kernel(MatmulIdParams p, int vec_ok) {
 constexpr int kMapThreads = 1024;
 constexpr int kMapWarps = kMapThreads / 32;
 constexpr int kMapBatch = 16;  // ids per lane held in registers per step
+constexpr int kMapCluster = 8; // CTAs of the cluster that builds the map
+
+// Lanes of the warp holding the same key: one ballot per key bit (keys are
+// below 2^nbits), AND-ed so that only lanes agreeing on every bit remain.
+__device__ __forceinline__ unsigned same_key_lanes(uint32_t key, int nbits) {
+    unsigned mask = 0xffffffffu;
+    for (int b = 0; b < nbits; ++b) {
+        const uint32_t bit = (key >> b) & 1u;
+        const unsigned bal = __ballot_sync(0xffffffffu, bit);
+        mask &= bit ? bal : ~bal;
+    }
+    return mask;
+}
 
 __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdParams p) {
     const int tid = threadIdx.x;
@@ -192,12 +272,12 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
     const uint32_t E = static_cast<uint32_t>(p.n_experts);
     const int64_t total = p.total_rows;
 
-    if (blockIdx.x > 0) {
+    if (static_cast<int>(blockIdx.x) >= kMapCluster) {
         // zero-fill output rows whose id is outside [0, n_experts)
         __shared__ uint32_t s_rows[kMapThreads];
         __shared__ int s_wc[kMapWarps];
-        for (int64_t base = static_cast<int64_t>(blockIdx.x - 1) * kMapThreads; base < total;
-             base += static_cast<int64_t>(gridDim.x - 1) * kMapThreads) {
+        const int64_t zb = blockIdx.x - kMapCluster, nz = gridDim.x - kMapCluster;
+        for (int64_t base = zb * kMapThreads; base < total; base += nz * kMapThreads) {
             const int64_t r = base + tid;
             const bool bad = r < total && p.ids[r] >= E;
             const unsigned bal = __ballot_sync(0xffffffffu, bad);
@@ -219,14 +299,24 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
         return;
     }
 
-    extern __shared__ uint32_t cnt[];  // [kMapWarps][E]
+    // the map proper: one cluster of kMapCluster CTAs, CTA c owns the c-th
+    // contiguous segment of routed rows, each of its warps a sub-segment
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = static_cast<int>(blockIdx.x);  // == rank in the first cluster
+    extern __shared__ uint32_t cnt[];  // [kMapWarps][E] counts, then tot[E]
+    uint32_t *tot = cnt + static_cast<int64_t>(kMapWarps) * E;
     uint32_t *mine = cnt + static_cast<int64_t>(warp) * E;
-    int64_t seg = (total + kMapWarps - 1) / kMapWarps;
-    seg = (seg + 31) / 32 * 32;
-    const int64_t beg = static_cast<int64_t>(warp) * seg;
-    const int64_t end = beg + seg < total ? beg + seg : total;
+    int64_t cseg = (total + kMapCluster - 1) / kMapCluster;
+    cseg = (cseg + 32 * kMapWarps - 1) / (32 * kMapWarps) * (32 * kMapWarps);
+    const int64_t cbeg = crank * cseg;
+    const int64_t cend = cbeg + cseg < total ? cbeg + cseg : total;
+    const int64_t wseg = cseg / kMapWarps;
+    const int64_t beg = cbeg + static_cast<int64_t>(warp) * wseg;
+    const int64_t end = beg + wseg < cend ? beg + wseg : cend;
     for (uint32_t e = lane; e < E; e += 32) mine[e] = 0;
     __syncwarp();
+    // keys 0..E-1 are experts, E marks an out-of-range id
+    const int nbits = 32 - __clz(static_cast<int>(E));
 
     // pass 1: per-warp counts
     for (int64_t base = beg; base < end; base += 32 * kMapBatch) {
@@ -238,15 +328,15 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
         }
 #pragma unroll
         for (int b = 0; b < kMapBatch; ++b) {
-            const uint32_t key = v[b] < E ? v[b] : 0xffffffffu;
-            const unsigned grp = __match_any_sync(0xffffffffu, key);
-            if (key != 0xffffffffu && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
+            const uint32_t key = v[b] < E ? v[b] : E;
+            const unsigned grp = same_key_lanes(key, nbits);
+            if (key != E && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
             __syncwarp();
         }
     }
     __syncthreads();
 
-    // exclusive scan across warps (row order) per expert; totals are the counts
+    // exclusive scan across this CTA's warps (row order) per expert
     for (uint32_t e = tid; e < E; e += kMapThreads) {
         uint32_t run = 0;
         for (int w = 0; w < kMapWarps; ++w) {
@@ -254,9 +344,17 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
             cnt[static_cast<int64_t>(w) * E + e] = run;
             run += c;
         }
-        p.counts[e] = run;
+        tot[e] = run;
     }
-    __syncthreads();
+    cluster.sync();  // every CTA's per-expert totals are visible cluster-wide
+    // rows of lower-ranked CTAs come first: read their totals through DSMEM
+    for (uint32_t e = tid; e < E; e += kMapThreads) {
+        uint32_t below = 0;
+        for (int c = 0; c < crank; ++c) below += cluster.map_shared_rank(tot, c)[e];
+        for (int w = 0; w < kMapWarps; ++w) cnt[static_cast<int64_t>(w) * E + e] += below;
+        if (crank == kMapCluster - 1) p.counts[e] = below + tot[e];
+    }
+    cluster.sync();  // remote reads done before any CTA moves on (and later exits)
 
     // pass 2: scatter row indices to their ascending positions
     const uint32_t lt_mask = (1u << lane) - 1u;
@@ -270,15 +368,15 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
 #pragma unroll
         for (int b = 0; b < kMapBatch; ++b) {
             const int64_t r = base + b * 32 + lane;
-            const uint32_t key = v[b] < E ? v[b] : 0xffffffffu;
-            const unsigned grp = __match_any_sync(0xffffffffu, key);
-            if (key != 0xffffffffu) {
+            const uint32_t key = v[b] < E ? v[b] : E;
+            const unsigned grp = same_key_lanes(key, nbits);
+            if (key != E) {
                 const uint32_t pos = mine[key] + __popc(grp & lt_mask);
                 if (pos < static_cast<uint32_t>(p.m))
                     p.routed_rows[static_cast<int64_t>(key) * p.m + pos] = static_cast<uint32_t>(r);
             }
             __syncwarp();
-            if (key != 0xffffffffu && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
+            if (key != E && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
             __syncwarp();
         }
     }
@@ -403,7 +501,7 @@ cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream
 }
 
 cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(kMapWarps) * static_cast<size_t>(p.n_experts) * 4;
+    const size_t smem = (static_cast<size_t>(kMapWarps) + 1) * static_cast<size_t>(p.n_experts) * 4;
     static unsigned long long attr_set = 0;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -411,16 +509,30 @@ cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s) {
     if (!(attr_set & bit)) {
         cudaError_t e = cudaFuncSetAttribute(matmul_id_map_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kMapWarps * 1024 * 4);
+                                             (kMapWarps + 1) * 1024 * 4);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
+    // the first cluster builds the map; the other clusters zero-fill the rows of
+    // out-of-range ids
     int64_t zero_ctas = (p.total_rows + kMapThreads - 1) / kMapThreads;
     const int64_t cap = 2LL * sm_count();
     if (zero_ctas > cap) zero_ctas = cap;
-    if (zero_ctas < 1) zero_ctas = 1;
-    matmul_id_map_kernel<<<static_cast<unsigned>(1 + zero_ctas), kMapThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    zero_ctas = (zero_ctas + kMapCluster - 1) / kMapCluster * kMapCluster;
+    if (zero_ctas < kMapCluster) zero_ctas = kMapCluster;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(kMapCluster + zero_ctas), 1, 1);
+    cfg.blockDim = dim3(kMapThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMapCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, matmul_id_map_kernel, p);
 }
 
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s) {

@@ -137,11 +137,15 @@ def test_tc_gemm_exact_small_integers(oracle_mod, dtype):
 
 @pytest.mark.parametrize("dtype", synth.DTYPES)
 @pytest.mark.parametrize("ta,tb", [(False, False), (False, True), (True, False), (True, True)])
-def test_general_gemm_parity(oracle_mod, dtype, ta, tb):
-    g = StridedGemm(dtype, 2, 70, 90, 45, ta, tb, lda=(70 if ta else 45) + 3,
-                    ldb=(45 if tb else 90) + 5, ldc=95, a_off=synth.ITEMSIZE[dtype] * 3)
-    # the odd offsets and leading dims rule out the TMA path for every dtype
-    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+@pytest.mark.parametrize("size,kernel", [((2, 70, 90, 45), "gbmm_gemm_small"),
+                                         ((2, 150, 170, 83), "gbmm_gemm_simt")])
+def test_general_gemm_parity(oracle_mod, dtype, ta, tb, size, kernel):
+    batch, m, n, k = size
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, lda=(m if ta else k) + 3,
+                    ldb=(k if tb else n) + 5, ldc=n + 5, a_off=synth.ITEMSIZE[dtype] * 3)
+    # the odd offsets and leading dims rule out the TMA path for every dtype;
+    # a few thousand outputs take the latency-bound kernel, more the tiled one
+    run_case(oracle_mod, g, expect_kernel=kernel)
 
 
 def test_f32_gemm_workload_c1(oracle_mod):
@@ -150,7 +154,7 @@ def test_f32_gemm_workload_c1(oracle_mod):
     g = StridedGemm("f32", 1, 64, 64, 128, False, False)
     g.a[:] = w.a.reshape(-1)
     g.b[:] = w.b.reshape(-1)
-    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_small")
 
 
 def test_f32_gemm_page_shapes(oracle_mod):
