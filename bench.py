@@ -395,6 +395,35 @@ def run_ours(args) -> None:
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms, "steps": e2e_steps}
 
+    # side measurement (not part of the step): the grouped workload with the
+    # opt-in single bf16 rounding of the activations, same buffers and order
+    single = None
+    if "c5" in probs and not args.no_options:
+        pc = probs["c5"]
+        default_precision = pc.params.activation_precision
+        pc.params.activation_precision = gb.ACT_BF16
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            pc.call(sptr)
+        times = []
+        for _ in range(max(3, args.steps // 2)):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pc.call(sptr)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        pc.params.activation_precision = default_precision
+        del flush
+        ms = statistics.median(times)
+        single = {"ms": ms, "roofline_ms": roof["c5"] * 1e3,
+                  "frac_of_roofline": roof["c5"] * 1e3 / ms,
+                  "note": "matmul_id GroupedPrefill with activation_precision=bf16 (opt-in: one "
+                          "bf16 rounding of the activations, half the tensor work; default splits "
+                          "x = hi + lo); timed alone after an L2 flush"}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -445,7 +474,8 @@ def run_ours(args) -> None:
                                                                    ("hbm_gbs", "bf16_tflops",
                                                                     "bf16_tflops_sustained")
                                                                    if k in peaks},
-                   "roofline_ms_per_step": roof_total * 1e3, "calls": calls},
+                   "roofline_ms_per_step": roof_total * 1e3, "calls": calls,
+                   "c5_single_rounding_option": single},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk, "wall_s_timed": wall,
     }
@@ -524,6 +554,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-scale", type=float, default=1.0)
+    ap.add_argument("--no-options", action="store_true", help="skip the opt-in mode side timings")
     args = ap.parse_args()
     args.only = [k.strip() for k in args.only.split(",") if k.strip()]
     if args.warmup < 3 and args.impl == "ours":

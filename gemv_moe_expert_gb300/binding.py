@@ -31,6 +31,7 @@ GBMM_F32, GBMM_F16, GBMM_BF16 = 0, 1, 2
 DTYPE_CODES = {"f32": GBMM_F32, "f16": GBMM_F16, "bf16": GBMM_BF16}
 
 INPUT_SHARED_PER_TOKEN, INPUT_SLOTTED = 0, 1
+ACT_SPLIT, ACT_BF16 = 0, 1
 IDS_DISTINCT_PER_TOKEN, IDS_MAY_REPEAT = 0, 1
 ROUTE_DIRECT, ROUTE_GROUPED_PREFILL = 0, 1
 MATMUL_ID_SCHEMA_VERSION = 3
@@ -54,7 +55,8 @@ class MatmulIdParams(ctypes.Structure):
     _fields_ = [("m", ctypes.c_uint32), ("n", ctypes.c_uint32), ("k", ctypes.c_uint32),
                 ("top_k", ctypes.c_uint32), ("n_experts", ctypes.c_uint32),
                 ("input_layout", ctypes.c_uint32), ("multiplicity", ctypes.c_uint32),
-                ("route", ctypes.c_uint32), ("expert_stride_bytes", ctypes.c_uint64)]
+                ("route", ctypes.c_uint32), ("expert_stride_bytes", ctypes.c_uint64),
+                ("activation_precision", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class MatmulIdCapability(ctypes.Structure):
@@ -196,9 +198,9 @@ def gbmm_matmul_id_scratch_bytes(max_experts: int, max_tokens: int):
 
 
 def make_params(m, n, k, top_k, n_experts, expert_stride_bytes, input_layout=0, multiplicity=0,
-                route=0) -> MatmulIdParams:
+                route=0, activation_precision=0) -> MatmulIdParams:
     return MatmulIdParams(m, n, k, top_k, n_experts, input_layout, multiplicity, route,
-                          expert_stride_bytes)
+                          expert_stride_bytes, activation_precision, 0)
 
 
 def gbmm_matmul_id_capability(weight_dtype, params: MatmulIdParams):

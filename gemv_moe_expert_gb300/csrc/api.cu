@@ -342,6 +342,9 @@ gbmm_status capability_impl(gbmm_dtype wdt, const gbmm_matmul_id_params *p,
         return fail(GBMM_ERR_INVALID_ARGUMENT, "%s: m, n, k, top_k and n_experts must be nonzero", fn);
     if (p->input_layout > 1 || p->multiplicity > 1 || p->route > 1)
         return fail(GBMM_ERR_INVALID_ARGUMENT, "%s: unknown layout, multiplicity or route", fn);
+    if (p->activation_precision > 1 || p->reserved != 0)
+        return fail(GBMM_ERR_INVALID_ARGUMENT, "%s: unknown activation precision or nonzero reserved field",
+                    fn);
     if (p->top_k > p->n_experts && p->multiplicity == GBMM_IDS_DISTINCT_PER_TOKEN)
         return fail(GBMM_ERR_INVALID_ARGUMENT, "%s: distinct top_k %u exceeds n_experts %u", fn,
                     p->top_k, p->n_experts);
@@ -571,14 +574,17 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
               p->n_experts <= static_cast<uint32_t>(grouped_tc_max_experts());
     if (tc) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-        // weights: (k, n, expert), 256 x 64 boxes, 128-byte swizzle
+        // weights: (k, n, expert), 256 x bk boxes; a box row of bk bf16 is one
+        // swizzle row (64 bytes -> 64-byte swizzle, 128 bytes -> 128-byte)
+        const int bk = grouped_tc_block_k();
         cuuint64_t wdims[3] = {p->k, p->n, p->n_experts};
         cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(p->k) * 2, p->expert_stride_bytes};
-        cuuint32_t wbox[3] = {static_cast<cuuint32_t>(grouped_tc_block_k()), 256u, 1u};
+        cuuint32_t wbox[3] = {static_cast<cuuint32_t>(bk), 256u, 1u};
         cuuint32_t estr[3] = {1u, 1u, 1u};
         tc = enc != nullptr &&
              enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), wdims, wstrides,
-                 wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
     if (tc) {
@@ -588,8 +594,10 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
     st = after_launch(launch_matmul_id_map(mp, stream), "gbmm_matmul_id_map", stream);
     if (st != GBMM_OK) return st;
     if (tc) {
-        const int out_vec_ok = aligned(out, 16) && p->n % 4 == 0;
-        st = after_launch(launch_matmul_id_grouped_tc(map_w, mp, out_vec_ok, device_sm_count(), stream),
+        // 2: 32-byte stores (rows 32-byte aligned), 1: 16-byte stores, 0: scalar
+        const int out_vec_ok = (aligned(out, 32) && p->n % 8 == 0) ? 2 : (aligned(out, 16) && p->n % 4 == 0) ? 1 : 0;
+        const int split = p->activation_precision == GBMM_ACT_SPLIT ? 1 : 0;
+        st = after_launch(launch_matmul_id_grouped_tc(map_w, mp, out_vec_ok, split, device_sm_count(), stream),
                           "gbmm_matmul_id_grouped_tc", stream);
     } else {
         st = after_launch(launch_matmul_id_grouped_simt(weight_dtype, mp, stream),

@@ -101,6 +101,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     return ready != 0;
 }
 
+// kSplit: activations as bf16 hi + lo (two MMAs per weight tile); without it
+// a single bf16 rounding (opt-in, half the tensor work).
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams p, int out_vec_ok) {
     extern __shared__ uint8_t smem_raw[];
@@ -265,7 +268,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                             const uint64_t dw = sdesc_kmajor_sw128(s_w0 + h * kWBytes + kk * 32);
                             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * kBNH);
                             umma_f16_ss(d_tmem, da_hi, dw, kIdesc, acc);
-                            umma_f16_ss(d_tmem, da_lo, dw, kIdesc, 1u);
+                            if (kSplit) umma_f16_ss(d_tmem, da_lo, dw, kIdesc, 1u);
                         }
                     }
                     umma_commit(empty_bar(stage));
@@ -313,7 +316,16 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 tmem_ld_wait();
                 const int64_t j0 = static_cast<int64_t>(g.nb) * kBN + chunk * 32;
                 if (valid && j0 < p.n) {
-                    if (out_vec_ok && j0 + 32 <= p.n) {
+                    if (out_vec_ok == 2 && j0 + 32 <= p.n) {
+                        // whole 32-byte sectors per store: no partial-sector writes in L2
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            asm volatile(
+                                "st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + j0 + 8 * q),
+                                "r"(v[8 * q]), "r"(v[8 * q + 1]), "r"(v[8 * q + 2]), "r"(v[8 * q + 3]),
+                                "r"(v[8 * q + 4]), "r"(v[8 * q + 5]), "r"(v[8 * q + 6]), "r"(v[8 * q + 7])
+                                : "memory");
+                    } else if (out_vec_ok && j0 + 32 <= p.n) {
                         float4 *dst = reinterpret_cast<float4 *>(orow + j0);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -399,7 +411,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         hi[h] = pack_bf16(f[2 * h], f[2 * h + 1]);
-                        lo[h] = pack_bf16(f[2 * h] - bf16_half(hi[h], 0), f[2 * h + 1] - bf16_half(hi[h], 1));
+                        if (kSplit)
+                            lo[h] = pack_bf16(f[2 * h] - bf16_half(hi[h], 0), f[2 * h + 1] - bf16_half(hi[h], 1));
                     }
                     // 128-byte swizzle: 16-byte chunk c of row i sits at chunk c ^ (i % 8)
                     const uint32_t off = static_cast<uint32_t>(i) * 128u +
@@ -407,9 +420,10 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + off), "r"(hi[0]),
                                  "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
                                  : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + kXBytes + off),
-                                 "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
-                                 : "memory");
+                    if (kSplit)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + kXBytes + off),
+                                     "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                                     : "memory");
                 }
                 fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
                 __syncwarp();
@@ -445,20 +459,29 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 
 }  // namespace
 
-cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
-                                        int num_sms, cudaStream_t s) {
+namespace {
+template <bool kSplit>
+cudaError_t grouped_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok, int num_sms,
+                         cudaStream_t s) {
     static unsigned long long attr_set = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<kSplit>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    grouped_tc_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(map_w, p, out_vec_ok);
+    grouped_tc_kernel<kSplit><<<num_sms, kThreads, kSmemBytes, s>>>(map_w, p, out_vec_ok);
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
+                                        int split, int num_sms, cudaStream_t s) {
+    return split ? grouped_tc_t<true>(map_w, p, out_vec_ok, num_sms, s)
+                 : grouped_tc_t<false>(map_w, p, out_vec_ok, num_sms, s);
 }
 
 int grouped_tc_max_experts() { return kMaxExperts; }

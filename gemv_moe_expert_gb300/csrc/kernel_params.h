@@ -100,7 +100,7 @@ cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream
 cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
-                                        int num_sms, cudaStream_t s);
+                                        int split, int num_sms, cudaStream_t s);
 cudaError_t launch_bounded_wait_test(uint32_t *err, uint64_t limit_ns, cudaStream_t s);
 int grouped_tc_max_experts();
 int grouped_tc_block_k();

@@ -148,7 +148,26 @@ typedef struct gbmm_matmul_id_params {
     uint32_t multiplicity; /* GBMM_IDS_* */
     uint32_t route;        /* GBMM_ROUTE_* */
     uint64_t expert_stride_bytes; /* bytes from expert e to expert e+1 */
+    /* GBMM_ACT_* (an extension of this library; zero = the pages' f32
+     * activation product).  Only the GroupedPrefill route with bf16 weights on
+     * the tensor cores reads it; elsewhere every value computes in f32. */
+    uint32_t activation_precision;
+    uint32_t reserved;     /* must be 0 */
 } gbmm_matmul_id_params;
+
+/*
+ * Activation precision of the tensor-core grouped GEMM (bf16 weights, f32
+ * activations).  Tensor cores multiply bf16 pairs, so the f32 activations
+ * must be rounded:
+ *   GBMM_ACT_SPLIT (default): x = hi + lo with hi = bf16(x), lo = bf16(x - hi),
+ *     both multiplied by the weights -- activation error <= 2^-16 |x|, the
+ *     product is f32-accurate and every element meets 2e-3 * sum|w||x|.
+ *   GBMM_ACT_BF16: x rounded once to bf16, half the tensor work -- activation
+ *     error <= 2^-8 |x|, so an element can differ from the f32 product by up
+ *     to ~2^-8 * sum|w||x| (about 3.9e-3, above the 2e-3 bound when all
+ *     products share a sign; far below it for zero-mean data).
+ */
+enum { GBMM_ACT_SPLIT = 0, GBMM_ACT_BF16 = 1 };
 
 /* [P2] `DenseMatmulIdCapability` + `DenseMatmulIdScratchRequirement` */
 typedef struct gbmm_matmul_id_capability_t {

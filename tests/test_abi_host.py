@@ -153,6 +153,16 @@ def test_capability_accepts_grouped_boundary_and_repeat_direct(lib):
     assert gb.gbmm_matmul_id_capability("bf16", p)[0] == gb.GBMM_OK
 
 
+def test_capability_activation_precision_field(lib):
+    p = gb.make_params(4, 8, 16, 2, 8, 8 * 16 * 2, route=1, activation_precision=gb.ACT_BF16)
+    assert gb.gbmm_matmul_id_capability("bf16", p)[0] == gb.GBMM_OK
+    p = gb.make_params(4, 8, 16, 2, 8, 8 * 16 * 2, activation_precision=2)
+    assert gb.gbmm_matmul_id_capability("bf16", p)[0] == gb.GBMM_ERR_INVALID_ARGUMENT
+    p = gb.make_params(4, 8, 16, 2, 8, 8 * 16 * 2)
+    p.reserved = 1
+    assert gb.gbmm_matmul_id_capability("bf16", p)[0] == gb.GBMM_ERR_INVALID_ARGUMENT
+
+
 def test_capability_rejects_unsupported_dtype(lib):
     p = gb.make_params(4, 8, 16, 2, 8, 8 * 16 * 2)
     st, _ = gb.gbmm_matmul_id_capability(7, p)

@@ -31,11 +31,11 @@ def _lib():
 class Run:
     """Uploads a MatmulIdCase, calls gbmm_matmul_id, reads results back."""
 
-    def __init__(self, case: synth.MatmulIdCase, out_fill=0x7F):
+    def __init__(self, case: synth.MatmulIdCase, out_fill=0x7F, precision=0):
         self.case = case
         c = case
         self.params = gb.make_params(c.m, c.n, c.k, c.top_k, c.n_experts, c.expert_stride_bytes,
-                                     c.input_layout, c.multiplicity, c.route)
+                                     c.input_layout, c.multiplicity, c.route, precision)
         st, cap = gb.gbmm_matmul_id_capability(c.wdtype, self.params)
         assert st == gb.GBMM_OK, gb.gbmm_last_error()
         self.cap = cap
@@ -201,3 +201,40 @@ def test_grouped_all_rows_one_expert(oracle_mod):
     ids[:, 1] = 1 + (np.arange(m) % 3)
     case = synth.matmul_id_case("one-expert", "bf16", m, 160, 192, top_k, E, route=1, ids=ids)
     Run(case).call().check(oracle_mod)
+
+
+def test_split_activations_meet_tolerance_where_single_rounding_cannot(oracle_mod):
+    """Activations at a bf16 rounding tie (1 + 2^-8, all positive) against positive
+    weights: a single bf16 rounding of x errs by ~3.9e-3 * sum|w||x|, above the
+    2e-3 bound, while the default hi/lo split (x = hi + lo exactly) meets it.
+    This is why the split is the default of the tensor-core grouped route."""
+    m, n, k, top_k, E = 64, 256, 512, 2, 4
+    case = synth.matmul_id_case("tie", "bf16", m, n, k, top_k, E, route=1, seed=2)
+    case.x[:] = np.float32(1.0 + 2.0 ** -8)
+    w = synth.bf16_bits_to_f32(case.w)
+    case.w[:] = synth.f32_to_bf16_bits(np.abs(w))
+    Run(case).call().check(oracle_mod)  # default: split, stated tolerance
+    fast = Run(case, precision=gb.ACT_BF16).call()
+    got = fast.output()
+    ref, ref_abs = oracle_mod.matmul_id("bf16", m, n, k, top_k, E, case.expert_stride_bytes, 0,
+                                        case.w, case.x, case.ids)
+    err = np.abs(got - ref.reshape(-1)) / ref_abs.reshape(-1)
+    assert err.max() > 2e-3          # a single rounding breaks the stated bound here
+    assert err.max() <= 2.0 ** -8 + 1e-5
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_grouped_single_rounding_mode(oracle_mod, layout):
+    """Opt-in single bf16 rounding of the activations: within its own bound
+    (2^-8 + 1e-5) * sum|w||x| everywhere, and on zero-mean data within the
+    stated 2e-3 bound too."""
+    case = synth.matmul_id_case("fast", "bf16", 300, 520, 1000, 4, 12, route=1,
+                                input_layout=layout, seed=7)
+    r = Run(case, precision=gb.ACT_BF16).call()
+    got = r.output()
+    ref, ref_abs = oracle_mod.matmul_id("bf16", case.m, case.n, case.k, case.top_k, case.n_experts,
+                                        case.expert_stride_bytes, layout, case.w, case.x, case.ids)
+    ref, ref_abs = ref.reshape(-1), ref_abs.reshape(-1)
+    assert np.all(np.abs(got - ref) <= (2.0 ** -8 + 1e-5) * ref_abs)
+    assert_close(got, ref, ref_abs, "bf16", "f32", "single-rounding mode, zero-mean data")
+    r.check_map(oracle_mod)
