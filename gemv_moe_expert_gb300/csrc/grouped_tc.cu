@@ -24,7 +24,8 @@
 // One persistent CTA per SM, 14 warps:
 //   warp 0     TMA: two 256x64 bf16 weight tiles of W_e per k-block (3-D
 //              tensor map over (k, n, expert), 128-byte swizzle, L2
-//              evict-first), with L2 prefetches issued a few k-blocks ahead
+//              evict-first) into a ring of its own, with L2 prefetches issued
+//              a few k-blocks ahead
 //   warp 1     TMEM allocation (512 columns) and the MMA issuer:
 //              16 x tcgen05.mma (M=128, N=256, K=16) per 64-wide k-block
 //   warps 2..5 epilogue: TMEM -> registers -> f32 rows of `out`, scattered to
@@ -33,7 +34,10 @@
 //              evict-last: each token row serves top_k experts) two k-blocks
 //              ahead of use, split into bf16 hi / lo, write the 128-byte-
 //              swizzled K-major smem layout the MMA descriptors expect.
-// Shared memory: 2 stages x (x_hi 16 KB + x_lo 16 KB + 2 weight tiles 64 KB).
+// Shared memory: an activation ring of 2 stages x (x_hi 16 KB + x_lo 16 KB)
+// and a weight ring of 4 stages x one 256x64 tile (32 KB).  The weight ring
+// runs a half k-block at a time: a weight stage is refilled as soon as the
+// MMAs of its half are done, three half-tiles ahead of its next use.
 // Tile list: every CTA derives it from expert_counts (written by the map
 // launch before this one): tiles ordered by expert, then row block, then
 // output block.  Every mbarrier wait is bounded; see gemm_tc.cu.
@@ -47,7 +51,8 @@ constexpr int kBM = 128;
 constexpr int kBNH = 256;          // one accumulator / one MMA N
 constexpr int kBN = 2 * kBNH;      // tile width
 constexpr int kBK = 64;
-constexpr int kStages = 2;
+constexpr int kXStages = 2;         // activation stages (x_hi + x_lo of one k-block)
+constexpr int kWStages = 4;         // weight stages (one 256-row half of a k-block)
 constexpr int kThreads = 448;
 constexpr int kRowsPerProducer = 4;  // 8 producer warps x 32 row groups x 4 = 128 rows
 constexpr int kProducerWarp0 = 6;
@@ -55,13 +60,18 @@ constexpr int kWPrefetch = 4;      // k-blocks of weight L2 prefetch ahead
 constexpr int kXPrefetch = 4;      // k-blocks of activation L2 prefetch ahead of the loads
 constexpr uint32_t kXBytes = kBM * kBK * 2;   // one bf16 half of the activation tile
 constexpr uint32_t kWBytes = kBNH * kBK * 2;  // one weight tile
-constexpr uint32_t kStageBytes = 2 * kXBytes + 2 * kWBytes;
+constexpr uint32_t kXStageBytes = 2 * kXBytes;
+constexpr uint32_t kWBase = kXStages * kXStageBytes;  // weight ring after the activation ring
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + (kMaxExperts + 8) * 4 + 256 + 1024;
+constexpr uint32_t kRingBytes = kWBase + kWStages * kWBytes;
+constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 4;
+constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 8 * kNumBars + 16 + 1024;
 
 struct GroupedTile {
     int e, mb, nb, rows;
+    int n0;      // first output column of the work unit
+    int halves;  // 256-column accumulator halves it computes (0: nothing to do)
 };
 
 // expert of tile t: the largest e with prefix[e] <= t (prefix has E+1 entries)
@@ -79,6 +89,22 @@ __device__ __forceinline__ GroupedTile decode_grouped(int t, const uint32_t *pre
     g.nb = local % nblk;
     const int cnt = min(static_cast<int>(counts[lo]), m);
     g.rows = min(kBM, cnt - g.mb * kBM);
+    return g;
+}
+
+// Work units.  Tiles [0, split_from) run whole; when the tile count does not
+// divide evenly over the CTAs, each tile from split_from on is cut into two
+// 256-column units, so no CTA runs more than half a tile longer than another.
+// A unit whose columns start at or past n computes nothing (halves = 0), and
+// a whole tile whose second half lies past n computes one half.
+__device__ __forceinline__ GroupedTile decode_unit(int u, int split_from, const uint32_t *prefix, int E, int nblk,
+                                                   const uint32_t *counts, int m, int64_t n) {
+    const bool cut = u >= split_from;
+    const int t = cut ? split_from + (u - split_from) / 2 : u;
+    GroupedTile g = decode_grouped(t, prefix, E, nblk, counts, m);
+    g.n0 = g.nb * kBN + (cut ? ((u - split_from) & 1) * kBNH : 0);
+    const int want = cut ? 1 : 2;
+    g.halves = g.n0 >= n ? 0 : (g.n0 + kBNH >= n ? 1 : want);
     return g;
 }
 
@@ -111,16 +137,19 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     const uint32_t s_base = raw_addr + pad;
-    // stage s at s_base + s*kStageBytes: x_hi, x_lo, weight tile 0, weight tile 1
-    uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes);
+    // activation stage s at s_base + s*kXStageBytes (x_hi, x_lo); weight stage
+    // s at s_base + kWBase + s*kWBytes
+    uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kRingBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(prefix + kMaxExperts + 8);
     const uint32_t bar0 = smem_addr(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    const uint32_t tfull_bar = bar0 + 8u * (2 * kStages);
-    const uint32_t tempty_bar = bar0 + 8u * (2 * kStages + 1);
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 3);
+    auto xfull_bar = [&](int s) { return bar0 + 8u * s; };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (kXStages + s); };
+    auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * kXStages + s); };
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (2 * kXStages + kWStages + s); };
+    const uint32_t tfull_bar = bar0 + 8u * (2 * kXStages + 2 * kWStages);
+    auto tempty_bar = [&](int h) { return tfull_bar + 8u * (1 + h); };  // one per accumulator half
+    const uint32_t drain_bar = tfull_bar + 24u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ uint32_t warp_tot[kThreads / 32];
 
@@ -132,12 +161,17 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     const uint64_t lim = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1 + 8);  // TMA thread's arrive + one arrive per producer warp
-            mbar_init(empty_bar(s), 1);     // MMA commit
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(xfull_bar(s), 8);   // one arrive per producer warp
+            mbar_init(xempty_bar(s), 1);  // MMA commit
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(wfull_bar(s), 1);   // TMA thread's arrive + the copy's bytes
+            mbar_init(wempty_bar(s), 1);  // MMA commit
         }
         mbar_init(tfull_bar, 1);
-        mbar_init(tempty_bar, 4);
+        mbar_init(tempty_bar(0), 4);
+        mbar_init(tempty_bar(1), 4);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -187,6 +221,10 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int num_tiles = static_cast<int>(prefix[E]);
+    const int grid = static_cast<int>(gridDim.x);
+    const int tail = num_tiles > grid ? num_tiles % grid : (2 * num_tiles <= grid ? num_tiles : 0);
+    const int split_from = num_tiles - tail;
+    const int num_units = split_from + 2 * tail;
     const int kblocks = static_cast<int>((p.k + kBK - 1) / kBK);
 
     if (warp == 0) {
@@ -196,42 +234,39 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
-                const int n0 = g.nb * kBN;
-                for (int kb = 0; kb < kWPrefetch && kb < kblocks; ++kb) {
-                    tma_prefetch_3d(&map_w, kb * kBK, n0, g.e);
-                    tma_prefetch_3d(&map_w, kb * kBK, n0 + kBNH, g.e);
-                }
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (kb + kWPrefetch < kblocks) {
-                        tma_prefetch_3d(&map_w, (kb + kWPrefetch) * kBK, n0, g.e);
-                        tma_prefetch_3d(&map_w, (kb + kWPrefetch) * kBK, n0 + kBNH, g.e);
-                    }
-                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, lim, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t s_w = s_base + stage * kStageBytes + 2 * kXBytes;
-                    mbar_arrive_expect_tx(full_bar(stage), 2 * kWBytes);
-                    tma_load_3d_hint(s_w, &map_w, full_bar(stage), kb * kBK, n0, g.e, pol);
-                    tma_load_3d_hint(s_w + kWBytes, &map_w, full_bar(stage), kb * kBK, n0 + kBNH, g.e, pol);
-                    ++issued;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
+                if (g.halves == 0) continue;
+                const int n0 = g.n0;
+                for (int kb = 0; kb < kWPrefetch && kb < kblocks; ++kb)
+                    for (int h = 0; h < g.halves; ++h) tma_prefetch_3d(&map_w, kb * kBK, n0 + h * kBNH, g.e);
+                for (int kb = 0; kb < kblocks && ok; ++kb) {
+                    if (kb + kWPrefetch < kblocks)
+                        for (int h = 0; h < g.halves; ++h)
+                            tma_prefetch_3d(&map_w, (kb + kWPrefetch) * kBK, n0 + h * kBNH, g.e);
+                    for (int h = 0; h < g.halves; ++h) {
+                        if (!mbar_wait_bounded(wempty_bar(stage), phase ^ 1u, lim, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(wfull_bar(stage), kWBytes);
+                        tma_load_3d_hint(s_base + kWBase + stage * kWBytes, &map_w, wfull_bar(stage), kb * kBK,
+                                         n0 + h * kBNH, g.e, pol);
+                        ++issued;
+                        if (++stage == kWStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
             }
             if (!ok) {
                 *abort_flag = 1;
                 report_device_error(p.err, kKidGroupedTc);
-                // the stage barriers also count producer-warp arrivals, so a stage
-                // whose copies landed may still read as incomplete: the bounded
-                // wait below then just runs out (the copies are long done)
-                for (int s = 0; s < kStages; ++s) {
-                    const uint32_t n_s = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
-                    if (n_s > 0) mbar_wait_bounded(full_bar(s), (n_s - 1u) & 1u, lim, nullptr);
+                // let the copies in flight land before the CTA can exit
+                for (int s = 0; s < kWStages; ++s) {
+                    const uint32_t n_s = issued / kWStages + (static_cast<uint32_t>(s) < issued % kWStages ? 1u : 0u);
+                    if (n_s > 0) mbar_wait_bounded(wfull_bar(s), (n_s - 1u) & 1u, lim, nullptr);
                 }
             }
         }
@@ -239,47 +274,55 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
             constexpr uint32_t kIdesc = idesc_f16(1u, kBM, kBNH);  // bf16 x bf16 -> f32
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int xs = 0, ws = 0;
+            uint32_t xph = 0, wph = 0, acc_phase[2] = {0u, 0u};
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                // both accumulators drained by the epilogue of the previous tile
-                if (!mbar_wait_bounded(tempty_bar, acc_phase ^ 1u, lim, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait_bounded(full_bar(stage), phase, lim, abort_flag)) {
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
+                if (g.halves == 0) continue;
+                for (int kb = 0; kb < kblocks && ok; ++kb) {
+                    if (!mbar_wait_bounded(xfull_bar(xs), xph, lim, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t s_hi = s_base + stage * kStageBytes;
+                    const uint32_t s_hi = s_base + xs * kXStageBytes;
                     const uint32_t s_lo = s_hi + kXBytes;
-                    const uint32_t s_w0 = s_hi + 2 * kXBytes;
+                    for (int h = 0; h < g.halves; ++h) {
+                        // accumulator half h drained by the epilogue of the previous unit
+                        if (kb == 0 && !mbar_wait_bounded(tempty_bar(h), acc_phase[h] ^ 1u, lim, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait_bounded(wfull_bar(ws), wph, lim, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t s_w = s_base + kWBase + ws * kWBytes;
+                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * kBNH);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t da_hi = sdesc_kmajor_sw128(s_hi + kk * 32);
-                        const uint64_t da_lo = sdesc_kmajor_sw128(s_lo + kk * 32);
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint64_t dw = sdesc_kmajor_sw128(s_w0 + h * kWBytes + kk * 32);
-                            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * kBNH);
-                            umma_f16_ss(d_tmem, da_hi, dw, kIdesc, acc);
-                            if (kSplit) umma_f16_ss(d_tmem, da_lo, dw, kIdesc, 1u);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint64_t dw = sdesc_kmajor_sw128(s_w + kk * 32);
+                            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                            umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_hi + kk * 32), dw, kIdesc, acc);
+                            if (kSplit) umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_lo + kk * 32), dw, kIdesc, 1u);
+                        }
+                        umma_commit(wempty_bar(ws));
+                        if (++ws == kWStages) {
+                            ws = 0;
+                            wph ^= 1u;
                         }
                     }
-                    umma_commit(empty_bar(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (!ok) break;
+                    umma_commit(xempty_bar(xs));
+                    if (++xs == kXStages) {
+                        xs = 0;
+                        xph ^= 1u;
                     }
                 }
                 if (!ok) break;
                 umma_commit(tfull_bar);
-                acc_phase ^= 1u;
+                for (int h = 0; h < g.halves; ++h) acc_phase[h] ^= 1u;
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -292,8 +335,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         // ---------------- epilogue (warps 2..5) ----------------
         const int quarter = warp & 3;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
+            if (g.halves == 0) continue;
             if (!warp_wait(tfull_bar, acc_phase, lim, abort_flag, lane)) {
                 if (lane == 0) {
                     *abort_flag = 1;
@@ -310,11 +354,11 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             float *orow = p.out + r * p.n;
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-            for (int chunk = 0; chunk < kBN / 32; ++chunk) {
+            for (int chunk = 0; chunk < g.halves * (kBNH / 32); ++chunk) {
                 uint32_t v[32];
                 tmem_ld32(t_addr + chunk * 32, v);
                 tmem_ld_wait();
-                const int64_t j0 = static_cast<int64_t>(g.nb) * kBN + chunk * 32;
+                const int64_t j0 = static_cast<int64_t>(g.n0) + chunk * 32;
                 if (valid && j0 < p.n) {
                     if (out_vec_ok == 2 && j0 + 32 <= p.n) {
                         // whole 32-byte sectors per store: no partial-sector writes in L2
@@ -338,10 +382,13 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                             if (j0 + c < p.n) orow[j0 + c] = __uint_as_float(v[c]);
                     }
                 }
+                if ((chunk + 1) % (kBNH / 32) == 0) {
+                    // this accumulator half is in registers or stored: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(chunk / (kBNH / 32)));
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar);
             acc_phase ^= 1u;
         }
     } else {
@@ -357,8 +404,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const GroupedTile g = decode_grouped(t, prefix, E, nblk, p.counts, m);
+        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
+            if (g.halves == 0) continue;
             const float *src[kRowsPerProducer];
 #pragma unroll
             for (int q = 0; q < kRowsPerProducer; ++q) {
@@ -394,14 +442,14 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 }
             };
             auto consume = [&](float4 (&buf)[kRowsPerProducer][2]) -> bool {
-                if (!warp_wait(empty_bar(stage), phase ^ 1u, lim, abort_flag, lane)) {
+                if (!warp_wait(xempty_bar(stage), phase ^ 1u, lim, abort_flag, lane)) {
                     if (lane == 0) {
                         *abort_flag = 1;
                         report_device_error(p.err, kKidGroupedTc);
                     }
                     return false;
                 }
-                const uint32_t s_hi = s_base + stage * kStageBytes;
+                const uint32_t s_hi = s_base + stage * kXStageBytes;
 #pragma unroll
                 for (int q = 0; q < kRowsPerProducer; ++q) {
                     const int i = rsub + 32 * q;
@@ -427,8 +475,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 }
                 fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_bar(stage));
-                if (++stage == kStages) {
+                if (lane == 0) mbar_arrive(xfull_bar(stage));
+                if (++stage == kXStages) {
                     stage = 0;
                     phase ^= 1u;
                 }

@@ -154,6 +154,18 @@ def test_grouped_tc_odd_shapes(oracle_mod):
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
 
 
+def test_grouped_tc_tail_units(oracle_mod):
+    """More 128 x 512 tiles than CTAs, not a multiple of them: the last tiles run
+    as 256-column halves, and with n = 1100 the second half of every last
+    column block lies past n and is skipped.  Every output and the map."""
+    m, top_k, E = 2048, 4, 8
+    case = synth.matmul_id_case("tail", "bf16", m, 1100, 264, top_k, E, route=1, seed=11)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    r.check_map(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+
+
 @pytest.mark.parametrize("route", [0, 1])
 def test_out_of_range_ids_give_zero_rows(oracle_mod, route):
     m, top_k, E = 40, 4, 9
