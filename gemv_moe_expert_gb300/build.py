@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libgbmm.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["api.cu", "gemv.cu", "gemm_simt.cu", "gemm_tc.cu", "grouped_tc.cu", "matmul_id.cu",
-           "misc.cu", "static_scratch.cu"]
+           "misc.cu", "static_scratch.cu", "stream.cu"]
 HEADERS = ["device_common.cuh", "kernel_params.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

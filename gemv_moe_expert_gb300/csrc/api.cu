@@ -258,6 +258,11 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
             g.vec_ok = g.mat_ks == 1 && g.vec_ks == 1 && a16(g.mat) && s16(g.mat_rs) &&
                        s16(g.mat_bs) && a16(g.vec) && s16(g.vec_bs) && (g.nvec == 1 || s16(g.vec_rr));
             if (!resolve("gbmm_gemv_rowdot")) return GBMM_ERR_KERNEL_UNAVAILABLE;
+            g.err = device_error_word();
+            g.wait_limit_ns = kWaitLimitNs;
+            if (g.err != nullptr && gemv_stream_eligible(dt, g))
+                return after_launch(launch_gemv_stream(dt, g, device_sm_count(), stream), "gbmm_gemv_stream",
+                                    stream);
             return after_launch(launch_gemv_rowdot(dt, g, stream), "gbmm_gemv_rowdot", stream);
         }
         g.vec_ok = g.mat_rs == 1 && a16(g.mat) && s16(g.mat_ks) && s16(g.mat_bs);

@@ -22,6 +22,7 @@ enum KernelId : uint32_t {
     kKidGemmTc = 1,
     kKidGroupedTc = 2,
     kKidBoundedWaitTest = 3,
+    kKidGemvStream = 4,
 };
 
 // default limit of a bounded device wait (1 s)
@@ -43,6 +44,8 @@ struct GemvParams {
     int64_t out_os, out_rr, out_bs;
     int32_t nvec;     // vectors sharing one pass over the matrix (1..16)
     int32_t vec_ok;   // 16-byte vector path legal (host-checked alignment)
+    uint32_t *err;            // device error word (streamed kernel's bounded waits)
+    uint64_t wait_limit_ns;
 };
 
 // General strided GEMM (FFMA pipe).  Same addressing as the public API.
@@ -92,6 +95,9 @@ cudaError_t launch_fill_zero(int dt, void *c, int64_t batch, int64_t m, int64_t 
                              int64_t sc, cudaStream_t s);
 cudaError_t launch_gemv_rowdot(int dt, const GemvParams &p, cudaStream_t s);
 cudaError_t launch_gemv_coldot(int dt, const GemvParams &p, cudaStream_t s);
+// staged-stream GEMV (stream.cu) and the shapes it takes
+bool gemv_stream_eligible(int dt, const GemvParams &p);
+cudaError_t launch_gemv_stream(int dt, const GemvParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_small(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,

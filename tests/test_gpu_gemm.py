@@ -194,7 +194,7 @@ def test_gemv_parity(oracle_mod, dtype, case, entry):
     g = StridedGemm(dtype, batch, m, n, k, ta, tb, std=1.0, seed=k)
     fn = gb.gbmm_gemv if entry == "gemv" else gb.gbmm_gemm
     ratio = run_case(oracle_mod, g, fn=fn)
-    assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_rowdot", "gbmm_gemv_coldot")
+    assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_rowdot", "gbmm_gemv_coldot", "gbmm_gemv_stream")
     assert ratio <= 1.0
 
 
@@ -204,6 +204,35 @@ def test_gemv_decode_workload_c2(oracle_mod):
     g = StridedGemm("f16", 1, 1, 11008, 4096, False, True)
     g.a[:] = w.a.reshape(-1)
     g.b[:] = w.b.reshape(-1)
+    run_case(oracle_mod, g, fn=gb.gbmm_gemv, expect_kernel="gbmm_gemv_stream")
+
+
+# (dtype, n, k, ldb, m, kernel): whole rows per 16 KB staging slot (one copy
+# when contiguous, one per row when padded), several vectors; rows longer than
+# a slot go to the load-in-registers kernel
+STREAM_CASES = [
+    ("f16", 1000, 4096, None, 1, "gbmm_gemv_stream"),     # two 8 KB rows per slot
+    ("f32", 301, 4096, None, 1, "gbmm_gemv_stream"),      # one 16 KB row per slot
+    ("bf16", 777, 1000, None, 1, "gbmm_gemv_stream"),     # eight 2000-byte rows per slot, ragged tail
+    ("bf16", 515, 1024, 1032, 3, "gbmm_gemv_stream"),     # padded rows (ldb > k): one copy per row
+    ("f16", 129, 6000, 6008, 2, "gbmm_gemv_stream"),      # padded, one 12000-byte row per slot
+    ("f32", 64, 16, None, 1, "gbmm_gemv_stream"),         # 64-byte rows, 256 per slot
+    ("f16", 5, 8, None, 7, "gbmm_gemv_stream"),           # fewer rows than CTAs
+    ("f32", 301, 5000, None, 1, "gbmm_gemv_rowdot"),      # 20000-byte rows
+    ("f16", 129, 12000, None, 2, "gbmm_gemv_rowdot"),     # 24000-byte rows
+]
+
+
+@pytest.mark.parametrize("case", STREAM_CASES, ids=[str(c[:5]) for c in STREAM_CASES])
+def test_gemv_stream_parity(oracle_mod, case):
+    dtype, n, k, ldb, m, kernel = case
+    g = StridedGemm(dtype, 1, m, n, k, False, True, ldb=ldb, seed=n)
+    run_case(oracle_mod, g, fn=gb.gbmm_gemv if m == 1 else gb.gbmm_gemm, expect_kernel=kernel)
+
+
+def test_gemv_stream_not_taken_for_batches(oracle_mod):
+    # batched GEMV (a different vector per batch): the load-in-registers kernel
+    g = StridedGemm("f16", 3, 1, 200, 512, False, True, seed=2)
     run_case(oracle_mod, g, fn=gb.gbmm_gemv, expect_kernel="gbmm_gemv_rowdot")
 
 
@@ -226,14 +255,15 @@ def test_wide_skinny_ramp(oracle_mod, dtype, m, n, k):
     g.b[:] = synth.ramp((n * k,), 2, dtype)
     run_case(oracle_mod, g)
     if dtype != "f32":
-        assert gb.gbmm_test_last_kernel() == "gbmm_gemv_rowdot"
+        assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_rowdot", "gbmm_gemv_stream")
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("m", list(range(2, 16)))
 def test_wide_skinny_random(oracle_mod, dtype, m):
     g = StridedGemm(dtype, 1, m, 256 + 3, 4096 + 8, False, True, lda=4096 + 16, ldc=300, seed=m)
-    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_rowdot")
+    # m vectors of 8208 bytes are staged in 64 KB of shared memory up to m = 7
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_stream" if m <= 7 else "gbmm_gemv_rowdot")
 
 
 # ---------------------------------------------------------------------------

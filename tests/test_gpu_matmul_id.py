@@ -102,6 +102,33 @@ def test_direct_decode_workload_c4(oracle_mod):
     """m=4, E=64, top_k=8 distinct uniform ids, k=2048, n=1408, bf16 W: every output."""
     r = Run(synth.workload("c4_moe_direct")).call()
     r.check(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_direct"
+
+
+@pytest.mark.parametrize("wdtype", synth.DTYPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_direct_parity_many_rows_per_expert(oracle_mod, wdtype, layout):
+    # SharedPerToken: 128 routed rows over 12 experts, ~11 rows per expert
+    # (several passes of 4 rows over a weight tile); Slotted: 24 rows.  Ragged
+    # 32-row weight tiles (n = 300), padded expert stride.
+    m = 16 if layout == 0 else 3
+    case = synth.matmul_id_case(f"ds-{wdtype}-{layout}", wdtype, m, 300, 520, 8, 12, route=0,
+                                input_layout=layout, stride_pad_elems=8, seed=21)
+    Run(case).call().check(oracle_mod)
+
+
+def test_direct_may_repeat_and_out_of_range(oracle_mod):
+    m, top_k, E = 12, 6, 5
+    rng = np.random.default_rng(4)
+    ids = rng.integers(0, E, size=(m, top_k)).astype(np.uint32)   # repeats within a token
+    ids[2, 3] = E
+    ids[9, 0] = 0xFFFFFFFF
+    case = synth.matmul_id_case("ds-rep", "bf16", m, 136, 256, top_k, E, route=0, multiplicity=1,
+                                ids=ids)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    out = r.output().reshape(m, top_k, -1)
+    assert np.all(out[2, 3] == 0.0) and np.all(out[9, 0] == 0.0)
 
 
 def test_grouped_prefill_workload_c5_sampled(oracle_mod):
