@@ -486,9 +486,8 @@ def run_ours(args) -> None:
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # bytes), by workload, for the kernel as it stands; absent until captured again
-# after a change to that kernel.  c5: grouped_tc_kernel<1>, 3.0090 GB read +
-# 0.1912 GB written, one full-set capture of the default-precision launch.
-TRAFFIC: dict = {"c5": 3_200_204_488}
+# after a change to that kernel.
+TRAFFIC: dict = {}
 
 
 # ---------------------------------------------------------------------------
