@@ -188,33 +188,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Gather four rows (row coordinates y0..y3, each box one row high) of a 2-D
-// tensor at column c0 into consecutive shared memory.
-__device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                 int32_t c0, int32_t y0, int32_t y1, int32_t y2,
-                                                 int32_t y3, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-        "l"(map), "r"(bar), "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "l"(policy)
-        : "memory");
-}
-
-// Prefetch into L2 only (no shared-memory destination, no completion):
-// four gathered rows of a 2-D tensor / one tile of a 3-D tensor.
-__device__ __forceinline__ void tma_prefetch_gather4(const CUtensorMap *map, int32_t c0, int32_t y0,
-                                                     int32_t y1, int32_t y2, int32_t y3) {
-    asm volatile(
-        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile::gather4 [%0, {%1, %2, %3, %4, %5}];" ::"l"(map),
-        "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-        : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
-                 "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 // Bring the 128-byte line holding p into L2, marked evict-last.
 __device__ __forceinline__ void prefetch_l2_evict_last(const void *p) {
     asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
