@@ -193,10 +193,16 @@ __device__ __forceinline__ void prefetch_l2_evict_last(const void *p) {
     asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
 
-// L2 cache policies: data read once (streamed) / data re-read by many CTAs.
+// L2 cache policies: data read once (streamed) / data re-read by a few CTAs
+// close together in time / data re-read by many CTAs.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 __device__ __forceinline__ uint64_t policy_evict_last() {

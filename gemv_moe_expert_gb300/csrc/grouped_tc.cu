@@ -24,7 +24,7 @@
 // One persistent CTA per SM, 14 warps:
 //   warp 0     TMA: two 256x64 bf16 weight tiles of W_e per k-block (3-D
 //              tensor map over (k, n, expert), 128-byte swizzle, L2
-//              evict-first) into a ring of its own.  No L2 prefetch of the
+//              evict-normal) into a ring of its own.  No L2 prefetch of the
 //              weights: with three stages in flight it only took TMA issue
 //              slots (3 % slower with a prefetch 4 k-blocks ahead)
 //   warp 1     TMEM allocation (512 columns) and the MMA issuer:
@@ -232,7 +232,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- weight tiles (TMA) ----------------
-            const uint64_t pol = policy_evict_first();
+            // evict-normal: the row blocks of an expert read its weight slab
+            // close together in time (evict-first measured 7 % slower)
+            const uint64_t pol = policy_evict_normal();
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             bool ok = true;
