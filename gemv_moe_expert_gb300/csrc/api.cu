@@ -121,20 +121,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Tensor map of a K-contiguous [batch][rows][k] 16-bit operand, box
-// [box_rows][64], 128-byte swizzle (the UMMA K-major SW128 layout).
-bool encode_kmajor(CUtensorMap *map, int dt, const void *base, int64_t k, int64_t rows,
-                   int64_t batch, int64_t ld, int64_t bs, bool bcast, uint32_t box_rows) {
+// Tensor map of a 16-bit operand stored [batch][outer][inner] with row pitch
+// ld elements, box [box_outer][64 inner], 128-byte swizzle: with inner = k
+// the UMMA K-major SW128 layout (box_outer = the tile's rows), with inner =
+// m or n the M/N-major one (box_outer = 64 k-rows).
+bool encode_operand(CUtensorMap *map, int dt, const void *base, int64_t inner, int64_t outer, int64_t batch,
+                    int64_t ld, int64_t bs, bool bcast, uint32_t box_outer) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const int size = 2;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows),
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                           static_cast<cuuint64_t>(bcast ? 1 : batch)};
     cuuint64_t row_bytes = static_cast<cuuint64_t>(ld) * size;
-    cuuint64_t batch_bytes = bcast ? row_bytes * static_cast<cuuint64_t>(rows)
+    cuuint64_t batch_bytes = bcast ? row_bytes * static_cast<cuuint64_t>(outer)
                                    : static_cast<cuuint64_t>(bs) * size;
     cuuint64_t strides[2] = {row_bytes, batch_bytes};
-    cuuint32_t box[3] = {64u, box_rows, 1u};
+    cuuint32_t box[3] = {64u, box_outer, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = fn(map, dt == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     3, const_cast<void *>(base), dims, strides, box, estr,
@@ -270,18 +272,24 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
         return after_launch(launch_gemv_coldot(dt, g, stream), "gbmm_gemv_coldot", stream);
     }
 
-    // ---- tensor-core GEMM ----
-    const bool tc_layout = (dt == GBMM_F16 || dt == GBMM_BF16) && !ta && tb && a16(pa) && a16(pb) &&
-                           s16(lda) && s16(ldb) && s16(sa) && s16(sb) && m < (1LL << 31) &&
-                           n < (1LL << 31) && k < (1LL << 31) && batch < (1LL << 31);
+    // ---- tensor-core GEMM (every transpose combination; each operand read as stored) ----
+    const bool tc_layout = (dt == GBMM_F16 || dt == GBMM_BF16) && a16(pa) && a16(pb) && s16(lda) && s16(ldb) &&
+                           s16(sa) && s16(sb) && m < (1LL << 31) && n < (1LL << 31) && k < (1LL << 31) &&
+                           batch < (1LL << 31);
     if (tc_layout) {
-        const int bm = gemm_tc_block_m(), bn = gemm_tc_block_n();
+        const int bm = gemm_tc_block_m(), bn = gemm_tc_block_n(), bk = gemm_tc_block_k();
         const int64_t tiles_m = (m + bm - 1) / bm, tiles_n = (n + bn - 1) / bn;
         const int64_t tiles = tiles_m * tiles_n * batch;
+        const bool a_bc = sa == 0 || batch == 1, b_bc = sb == 0 || batch == 1;
+        // A: [m, k] K-contiguous, or stored [k, m] when transposed; B: [n, k]
+        // K-contiguous when transposed, else stored [k, n]
         CUtensorMap map_a, map_b;
-        if (tiles < (1LL << 31) &&
-            encode_kmajor(&map_a, dt, pa, k, m, batch, lda, sa, sa == 0 || batch == 1, bm) &&
-            encode_kmajor(&map_b, dt, pb, k, n, batch, ldb, sb, sb == 0 || batch == 1, bn)) {
+        const bool maps_ok =
+            (ta ? encode_operand(&map_a, dt, pa, m, k, batch, lda, sa, a_bc, static_cast<uint32_t>(bk))
+                : encode_operand(&map_a, dt, pa, k, m, batch, lda, sa, a_bc, static_cast<uint32_t>(bm))) &&
+            (tb ? encode_operand(&map_b, dt, pb, k, n, batch, ldb, sb, b_bc, static_cast<uint32_t>(bn))
+                : encode_operand(&map_b, dt, pb, n, k, batch, ldb, sb, b_bc, static_cast<uint32_t>(bk)));
+        if (tiles < (1LL << 31) && maps_ok) {
             if (!resolve("gbmm_gemm_tc")) return GBMM_ERR_KERNEL_UNAVAILABLE;
             uint32_t *err = device_error_word();
             if (err == nullptr) return fail(GBMM_ERR_CUDA, "%s: device error word unavailable", fn);
@@ -293,8 +301,10 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
             p.n = static_cast<int32_t>(n);
             p.k = static_cast<int32_t>(k);
             p.batch = static_cast<int32_t>(batch);
-            p.a_bcast = (sa == 0 || batch == 1) ? 1 : 0;
-            p.b_bcast = (sb == 0 || batch == 1) ? 1 : 0;
+            p.a_bcast = a_bc ? 1 : 0;
+            p.b_bcast = b_bc ? 1 : 0;
+            p.a_mn = ta ? 1 : 0;
+            p.b_mn = tb ? 0 : 1;
             p.c_vec_ok = (a16(pc) && s16(ldc) && s16(sc)) ? 1 : 0;
             p.tiles_m = static_cast<int32_t>(tiles_m);
             p.tiles_n = static_cast<int32_t>(tiles_n);

@@ -292,10 +292,28 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t saddr) {
     return d;
 }
 
+// M/N-major operand (the M or N dimension contiguous) with 128-byte
+// swizzling: each k-row holds 64 consecutive 16-bit M/N elements (128 bytes),
+// 8 k-rows form a 1024-byte swizzle atom; atoms along M/N are `mn_stride`
+// bytes apart (leading byte offset) and 8-row k-groups 1024 bytes apart
+// (stride byte offset).  Advancing K by 16 moves the start by 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: f32 accumulator, A/B format
-// (0 = f16, 1 = bf16), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_format, uint32_t m, uint32_t n) {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+// (0 = f16, 1 = bf16), A / B M- or N-major when a_mn / b_mn is set (bits 15,
+// 16; K-major otherwise), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_format, uint32_t m, uint32_t n, uint32_t a_mn = 0,
+                                                 uint32_t b_mn = 0) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
+           ((m >> 4) << 24);
 }
 
 // Each thread of the warp reads its TMEM lane (32 lanes per warp quarter),

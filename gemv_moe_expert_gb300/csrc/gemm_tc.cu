@@ -1,6 +1,9 @@
 // gemm_tc.cu -- batched f16/bf16 GEMM on the sm_103a tensor cores:
-// C[b] = A[b] * B[b]^T with A [m, k] and B [n, k] both K-contiguous (the
-// transpose_b layout), f32 accumulation in tensor memory, f16/bf16 output.
+// C[b] = op(A[b]) * op(B[b]) for every combination of the transpose flags,
+// f32 accumulation in tensor memory, f16/bf16 output.  Each operand is read
+// as stored: K-contiguous (A [m, k] untransposed, B [n, k] transposed) or
+// M/N-contiguous (A stored [k, m], B stored [k, n]); the MMA takes either
+// major-ness from its instruction descriptor.
 //
 // Semantics: tract-metal 0.23.6, src/kernels/matmul/mlx_gemm/mod.rs,
 // `dispatch_metal_mlx_gemm` (B stored [n, k] when transposed; batch strides
@@ -8,7 +11,9 @@
 //
 // Design (one persistent CTA per SM, 6 warps, warp-specialised):
 //   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles, 128-byte
-//               swizzled, into a 4-stage shared-memory ring (48 KB/stage).
+//               swizzled, into a 4-stage shared-memory ring (48 KB/stage);
+//               a K-major tile is one box of 64 k x 128 / 256 rows, an
+//               M/N-major tile two / four boxes of 64 m-or-n x 64 k, 8 KB apart.
 //   warp 1      allocates 512 TMEM columns (two 128x256 f32 accumulators)
 //               and issues tcgen05.mma (M=128, N=256, K=16) from one thread;
 //               tcgen05.commit releases a stage when its MMAs are done and
@@ -36,6 +41,7 @@ constexpr int kGroupM = 8;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kMNBox = 64 * kBK * 2;  // one 64 (m or n) x 64 (k) box of an M/N-major tile
 constexpr uint32_t kSmemBytes = kStages * (kABytes + kBBytes) + 256 + 1024;
 
 struct TileCoord {
@@ -69,7 +75,8 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <typename TC, uint32_t kFmt>
+// kAMN / kBMN: A / B stored M- / N-contiguous (see the file comment)
+template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const GemmTcParams p) {
@@ -135,10 +142,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(stage), kABytes + kBBytes);
-                    tma_load_3d(s_a + stage * kABytes, &map_a, full_bar(stage), kb * kBK, tc.mb * kBM,
-                                p.a_bcast ? 0 : tc.bat);
-                    tma_load_3d(s_b + stage * kBBytes, &map_b, full_bar(stage), kb * kBK, tc.nb * kBN,
-                                p.b_bcast ? 0 : tc.bat);
+                    const int abat = p.a_bcast ? 0 : tc.bat, bbat = p.b_bcast ? 0 : tc.bat;
+                    if (kAMN) {
+#pragma unroll
+                        for (int j = 0; j < kBM / 64; ++j)
+                            tma_load_3d(s_a + stage * kABytes + j * kMNBox, &map_a, full_bar(stage),
+                                        tc.mb * kBM + j * 64, kb * kBK, abat);
+                    } else {
+                        tma_load_3d(s_a + stage * kABytes, &map_a, full_bar(stage), kb * kBK, tc.mb * kBM, abat);
+                    }
+                    if (kBMN) {
+#pragma unroll
+                        for (int j = 0; j < kBN / 64; ++j)
+                            tma_load_3d(s_b + stage * kBBytes + j * kMNBox, &map_b, full_bar(stage),
+                                        tc.nb * kBN + j * 64, kb * kBK, bbat);
+                    } else {
+                        tma_load_3d(s_b + stage * kBBytes, &map_b, full_bar(stage), kb * kBK, tc.nb * kBN, bbat);
+                    }
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -159,7 +179,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t kIdesc = idesc_f16(kFmt, kBM, kBN);
+            constexpr uint32_t kIdesc = idesc_f16(kFmt, kBM, kBN, kAMN ? 1u : 0u, kBMN ? 1u : 0u);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -180,8 +200,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t da = sdesc_kmajor_sw128(s_a + stage * kABytes + kk * 32);
-                        const uint64_t db = sdesc_kmajor_sw128(s_b + stage * kBBytes + kk * 32);
+                        const uint64_t da = kAMN ? sdesc_mnmajor_sw128(s_a + stage * kABytes + kk * 2048, kMNBox)
+                                                 : sdesc_kmajor_sw128(s_a + stage * kABytes + kk * 32);
+                        const uint64_t db = kBMN ? sdesc_mnmajor_sw128(s_b + stage * kBBytes + kk * 2048, kMNBox)
+                                                 : sdesc_kmajor_sw128(s_b + stage * kBBytes + kk * 32);
                         umma_f16_ss(d_tmem, da, db, kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
@@ -269,7 +291,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
 }
 
-template <typename TC, uint32_t kFmt>
+template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
 cudaError_t tc_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
                  cudaStream_t s) {
     static unsigned long long attr_set = 0;  // one bit per device
@@ -277,14 +299,23 @@ cudaError_t tc_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParam
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<TC, kFmt>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<TC, kFmt, kAMN, kBMN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
     const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
-    gemm_tc_kernel<TC, kFmt><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
+    gemm_tc_kernel<TC, kFmt, kAMN, kBMN><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+template <typename TC, uint32_t kFmt>
+cudaError_t tc_major(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
+                     cudaStream_t s) {
+    if (p.a_mn) return p.b_mn ? tc_t<TC, kFmt, true, true>(ma, mb, p, num_sms, s)
+                              : tc_t<TC, kFmt, true, false>(ma, mb, p, num_sms, s);
+    return p.b_mn ? tc_t<TC, kFmt, false, true>(ma, mb, p, num_sms, s)
+                  : tc_t<TC, kFmt, false, false>(ma, mb, p, num_sms, s);
 }
 
 }  // namespace
@@ -296,8 +327,8 @@ int gemm_tc_block_k() { return kBK; }
 cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                            const GemmTcParams &p, int num_sms, cudaStream_t s) {
     switch (dt) {
-    case kF16: return tc_t<__half, 0>(map_a, map_b, p, num_sms, s);
-    case kBF16: return tc_t<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
+    case kF16: return tc_major<__half, 0>(map_a, map_b, p, num_sms, s);
+    case kBF16: return tc_major<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -59,13 +59,16 @@ struct GemmParams {
     int32_t ta, tb;
 };
 
-// Tensor-core GEMM: A [batch][m][k] and B [batch][n][k], K-contiguous, read by
-// TMA through the two tensor maps; C written with ldc / sc.
+// Tensor-core GEMM: A and B read by TMA through the two tensor maps, each
+// K-contiguous (A [batch][m][k], B [batch][n][k]) or, when a_mn / b_mn is
+// set, M/N-contiguous (A [batch][k][m], B [batch][k][n]); C written with
+// ldc / sc.
 struct GemmTcParams {
     void *c;
     int64_t ldc, sc;
     int32_t m, n, k, batch;
     int32_t a_bcast, b_bcast;   // batch stride 0: always batch coordinate 0
+    int32_t a_mn, b_mn;         // operand stored M- / N-contiguous
     int32_t c_vec_ok;           // C rows allow 16-byte stores
     int32_t tiles_m, tiles_n;
     int32_t num_tiles;

@@ -84,7 +84,7 @@ def test_worked_examples(oracle_mod, dtype):
 
 
 # ---------------------------------------------------------------------------
-# tensor-core GEMM (f16/bf16, A [m,k], B stored [n,k])
+# tensor-core GEMM (f16/bf16, every transpose combination)
 # ---------------------------------------------------------------------------
 
 TC_SHAPES = [
@@ -102,6 +102,44 @@ TC_SHAPES = [
 def test_tc_gemm_parity(oracle_mod, dtype, shape):
     batch, m, n, k = shape
     g = StridedGemm(dtype, batch, m, n, k, False, True, std=1.0 / np.sqrt(k), seed=batch + m)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
+def _up8(v):
+    return (v + 7) // 8 * 8
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("ta,tb", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=[str(s) for s in TC_SHAPES])
+def test_tc_gemm_transposes(oracle_mod, dtype, ta, tb, shape):
+    # operands read as stored: A [k, m] when ta (M-contiguous), B [k, n] when
+    # not tb (N-contiguous); leading dims rounded up to 8 elements for TMA,
+    # plus padding on one of them
+    batch, m, n, k = shape
+    lda = _up8(m if ta else k) + (8 if ta else 0)
+    ldb = _up8(k if tb else n) + (0 if tb else 16)
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, lda=lda, ldb=ldb, std=1.0 / np.sqrt(k),
+                    seed=batch + m + 7 * ta + 3 * tb)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("ta,tb", [(False, False), (True, False), (True, True)])
+def test_tc_gemm_transposes_exact_and_broadcast(oracle_mod, dtype, ta, tb):
+    # small integers: every partial sum exact, so every layout must agree with
+    # the oracle to the output rounding; and a broadcast operand (stride 0)
+    g = StridedGemm(dtype, 1, 256, 512, 1024, ta, tb, dist="ints", seed=5)
+    a, b, c = g.device()
+    assert gb.gbmm_gemm(*g.args(a, b, c)) == gb.GBMM_OK
+    assert gb.gbmm_test_last_kernel() == "gbmm_gemm_tc"
+    got = g.gather_c(c)
+    ref, _ = g.oracle(oracle_mod)
+    rounded = to_f64(synth._store(ref.astype(np.float32).reshape(-1), dtype), dtype).reshape(ref.shape)
+    assert np.array_equal(got, rounded)
+    rows_a, cols_a = (1000, 136) if ta else (136, 1000)
+    g = StridedGemm(dtype, 3, 136, 200, 1000, ta, tb, lda=_up8(cols_a), ldb=_up8(1000 if tb else 200),
+                    sa=0 if ta else None, sb=None if ta else 0, seed=9)
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
 
 
