@@ -546,6 +546,66 @@ def cpu_baseline_keys(workloads, keys, roof_total, scale):
             "sample": "sampled outputs per call (" + ", ".join(parts) + ")"}
 
 
+# ---------------------------------------------------------------------------
+# Direct vs GroupedPrefill crossover (the caller picks the route)
+# ---------------------------------------------------------------------------
+
+def run_crossover(args) -> None:
+    """Both expert-ID routes on the grouped workload's expert stack (128
+    experts of bf16 [1536, 4096], top-8 Zipf(1.1) ids, SharedPerToken f32 x)
+    for m = 1 .. 512 tokens, each call timed alone after an L2 flush (median of
+    --steps calls).  Prints one JSON line with the table and the first m at
+    which GroupedPrefill is faster, for callers that choose the route."""
+    import torch
+    from gemv_moe_expert_gb300 import binding as gb
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+    E, top_k, k, n = 128, 8, 4096, 1536
+    stride = n * k * 2
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w = (torch.randn(E * n * k, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    rows = []
+    for m in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
+        ids_h = synth.distinct_ids(m, top_k, E, seed=m, zipf_s=1.1)
+        ids = torch.from_numpy(ids_h.view(np.int32).reshape(-1).copy()).cuda()
+        x = torch.randn(m * k, device="cuda", generator=g)
+        out = torch.empty(m * top_k * n, device="cuda")
+        entry = {"m": m, "distinct_experts": int(len(np.unique(ids_h)))}
+        for route, name in ((gb.ROUTE_DIRECT, "direct_us"), (gb.ROUTE_GROUPED_PREFILL, "grouped_us")):
+            p = gb.make_params(m, n, k, top_k, E, stride, 0, 0, route)
+            st, cap = gb.gbmm_matmul_id_capability("bf16", p)
+            gb.check(st)
+            sc = None
+            if route == gb.ROUTE_GROUPED_PREFILL:
+                cnt = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device="cuda")
+                rr = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device="cuda")
+                sc = gb.make_scratch(cnt, cap.expert_counts_bytes, rr, cap.routed_rows_bytes, E, m)
+
+            def call():
+                gb.check(gb.gbmm_matmul_id(p, "bf16", w, w.numel() * 2, x, x.numel() * 4, ids, ids.numel() * 4,
+                                           out, out.numel() * 4, sc)[0])
+            for _ in range(args.warmup):
+                call()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(args.steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            entry[name] = statistics.median(ts)
+        rows.append(entry)
+    cross = next((r["m"] for r in rows if r["grouped_us"] < r["direct_us"]), None)
+    print(json.dumps({"sweep": "matmul_id route crossover", "experts": E, "top_k": top_k, "k": k, "n": n,
+                      "weights": "bf16", "ids": "top-8 distinct Zipf(1.1)", "rows": rows,
+                      "grouped_faster_from_m": cross}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -557,11 +617,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-scale", type=float, default=1.0)
     ap.add_argument("--no-options", action="store_true", help="skip the opt-in mode side timings")
+    ap.add_argument("--sweep", choices=["crossover"], default=None,
+                    help="instead of the step: time Direct against GroupedPrefill for m = 1..512")
     args = ap.parse_args()
     args.only = [k.strip() for k in args.only.split(",") if k.strip()]
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.sweep == "crossover":
+        run_crossover(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

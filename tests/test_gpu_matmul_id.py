@@ -107,6 +107,31 @@ def test_direct_decode_workload_c4(oracle_mod):
 
 @pytest.mark.parametrize("wdtype", synth.DTYPES)
 @pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("k", [256, 1024])
+def test_direct_parity_row_sizes(oracle_mod, wdtype, layout, k):
+    # 512 B to 4 KB weight rows, SharedPerToken with 128 routed rows (~11 per
+    # expert) or Slotted with 16, ragged n, padded expert stride
+    m = 16 if layout == 0 else 2
+    case = synth.matmul_id_case(f"dr-{wdtype}-{layout}-{k}", wdtype, m, 300, k, 8, 12, route=0,
+                                input_layout=layout, stride_pad_elems=8, seed=k + layout)
+    Run(case).call().check(oracle_mod)
+
+
+def test_direct_repeats_and_out_of_range_short_rows(oracle_mod):
+    m, top_k, E = 12, 6, 5
+    rng = np.random.default_rng(14)
+    ids = rng.integers(0, E, size=(m, top_k)).astype(np.uint32)   # repeats within a token
+    ids[1, 2] = E
+    ids[11, 5] = 0xFFFFFFFF
+    case = synth.matmul_id_case("dr-rep", "bf16", m, 136, 512, top_k, E, route=0, multiplicity=1, ids=ids)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    out = r.output().reshape(m, top_k, -1)
+    assert np.all(out[1, 2] == 0.0) and np.all(out[11, 5] == 0.0)
+
+
+@pytest.mark.parametrize("wdtype", synth.DTYPES)
+@pytest.mark.parametrize("layout", [0, 1])
 def test_direct_parity_many_rows_per_expert(oracle_mod, wdtype, layout):
     # SharedPerToken: 128 routed rows over 12 experts, ~11 rows per expert
     # (several passes of 4 rows over a weight tile); Slotted: 24 rows.  Ragged
