@@ -22,7 +22,10 @@
 //               output dtype, store; then hand the accumulator back, so the
 //               next tile's MMAs overlap this tile's stores.
 // Tiles are visited in a grouped raster (8 m-blocks x all n-blocks per group)
-// so the CTAs running at the same time share A and B panels in L2.
+// so the CTAs running at the same time share A and B panels in L2.  When the
+// last round of tiles would leave at least half of the CTAs idle, each of its
+// tiles runs as two 128x128 half units (N = 128 MMAs, the same rate per
+// column), so that round takes half a tile's time.
 // Every mbarrier wait is bounded; on a timeout the kernel records it in the
 // device error word, waits (bounded) for its own copies and MMAs in flight,
 // releases its TMEM and returns.
@@ -46,6 +49,8 @@ constexpr uint32_t kSmemBytes = kStages * (kABytes + kBBytes) + 256 + 1024;
 
 struct TileCoord {
     int bat, mb, nb;
+    int h;       // half of the tile's columns a half unit computes
+    int halves;  // 2: whole tile, 1: half unit h, 0: nothing (half past n)
 };
 
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmTcParams &p) {
@@ -59,6 +64,26 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmTcParams &p
     const int local = r % (kGroupM * p.tiles_n);
     t.mb = first_m + local % gm;
     t.nb = local / gm;
+    t.h = 0;
+    t.halves = 2;
+    return t;
+}
+
+// Tiles that do not split over the grid evenly: with tail = num_tiles mod
+// grid at most grid / 2, units [0, split_from) are whole tiles and every
+// tile from split_from on becomes two half units (units split_from + 2i and
+// split_from + 2i + 1).
+__device__ __forceinline__ int gemm_tail_tiles(int num_tiles, int grid) {
+    int tail = num_tiles > grid ? num_tiles % grid : (2 * num_tiles <= grid ? num_tiles : 0);
+    if (2 * tail > grid) tail = 0;
+    return tail;
+}
+
+__device__ __forceinline__ TileCoord decode_unit(int u, int split_from, const GemmTcParams &p) {
+    if (u < split_from) return decode_tile(u, p);
+    TileCoord t = decode_tile(split_from + (u - split_from) / 2, p);
+    t.h = (u - split_from) & 1;
+    t.halves = static_cast<int64_t>(t.nb) * kBN + t.h * (kBN / 2) < p.n ? 1 : 0;
     return t;
 }
 
@@ -126,6 +151,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kblocks = (p.k + kBK - 1) / kBK;
+    const int tail = gemm_tail_tiles(p.num_tiles, static_cast<int>(gridDim.x));
+    const int split_from = p.num_tiles - tail;
+    const int num_units = split_from + 2 * tail;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -134,8 +162,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             uint32_t phase = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-                const TileCoord tc = decode_tile(tile, p);
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                const TileCoord tc = decode_unit(u, split_from, p);
+                if (tc.halves == 0) continue;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
                         ok = false;
@@ -180,12 +209,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
             constexpr uint32_t kIdesc = idesc_f16(kFmt, kBM, kBN, kAMN ? 1u : 0u, kBMN ? 1u : 0u);
+            constexpr uint32_t kIdescHalf = idesc_f16(kFmt, kBM, kBN / 2, kAMN ? 1u : 0u, kBMN ? 1u : 0u);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                const TileCoord tc = decode_unit(u, split_from, p);
+                if (tc.halves == 0) continue;
+                // a half unit multiplies by B rows [h * 128, h * 128 + 128) of the
+                // stage: 16 KB further on in both B layouts
+                const uint32_t b_off = static_cast<uint32_t>(tc.h) * (kBBytes / 2);
+                const uint32_t idesc = tc.halves == 2 ? kIdesc : kIdescHalf;
                 if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p.wait_limit_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -202,9 +238,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t da = kAMN ? sdesc_mnmajor_sw128(s_a + stage * kABytes + kk * 2048, kMNBox)
                                                  : sdesc_kmajor_sw128(s_a + stage * kABytes + kk * 32);
-                        const uint64_t db = kBMN ? sdesc_mnmajor_sw128(s_b + stage * kBBytes + kk * 2048, kMNBox)
-                                                 : sdesc_kmajor_sw128(s_b + stage * kBBytes + kk * 32);
-                        umma_f16_ss(d_tmem, da, db, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        const uint64_t db = kBMN ? sdesc_mnmajor_sw128(s_b + stage * kBBytes + b_off + kk * 2048, kMNBox)
+                                                 : sdesc_kmajor_sw128(s_b + stage * kBBytes + b_off + kk * 32);
+                        umma_f16_ss(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == kStages) {
@@ -230,8 +266,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            const TileCoord tc = decode_tile(tile, p);
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const TileCoord tc = decode_unit(u, split_from, p);
+            if (tc.halves == 0) continue;
             // one lane waits and the warp follows its verdict, so the warp stays
             // converged for the .sync.aligned TMEM loads below
             int ready = 0;
@@ -251,11 +288,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                     static_cast<uint32_t>(acc * kBN);
 #pragma unroll 1
-            for (int chunk = 0; chunk < kBN / 32; ++chunk) {
+            for (int chunk = 0; chunk < tc.halves * (kBN / 64); ++chunk) {
                 uint32_t r[32];
                 tmem_ld32(t_addr + chunk * 32, r);
                 tmem_ld_wait();
-                const int64_t col0 = static_cast<int64_t>(tc.nb) * kBN + chunk * 32;
+                const int64_t col0 = static_cast<int64_t>(tc.nb) * kBN + tc.h * (kBN / 2) + chunk * 32;
                 if (row < p.m && col0 < p.n) {
                     if (p.c_vec_ok && col0 + 32 <= p.n) {
                         uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
@@ -304,7 +341,8 @@ cudaError_t tc_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParam
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    // at most half an SM's worth of tiles: every tile runs as two half units
+    const int grid = 2 * p.num_tiles <= num_sms ? 2 * p.num_tiles : (p.num_tiles < num_sms ? p.num_tiles : num_sms);
     gemm_tc_kernel<TC, kFmt, kAMN, kBMN><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
     return cudaGetLastError();
 }

@@ -20,7 +20,7 @@
 // Routing map.  One cluster of 8 CTAs x 32 warps builds expert_counts and
 // routed_rows without atomics: each warp owns a contiguous segment of routed
 // rows and counts it per expert (lanes holding the same id are found with
-// one warp ballot per id bit; one leader lane per distinct id updates the
+// one warp match instruction; one leader lane per distinct id updates the
 // warp's private counter row in shared memory), the per
 // expert counts are scanned across warps and, through distributed shared
 // memory, across the cluster's CTAs in row order, and a second pass
@@ -253,18 +253,6 @@ constexpr int kMapWarps = kMapThreads / 32;
 constexpr int kMapBatch = 16;  // ids per lane held in registers per step
 constexpr int kMapCluster = 8; // CTAs of the cluster that builds the map
 
-// Lanes of the warp holding the same key: one ballot per key bit (keys are
-// below 2^nbits), AND-ed so that only lanes agreeing on every bit remain.
-__device__ __forceinline__ unsigned same_key_lanes(uint32_t key, int nbits) {
-    unsigned mask = 0xffffffffu;
-    for (int b = 0; b < nbits; ++b) {
-        const uint32_t bit = (key >> b) & 1u;
-        const unsigned bal = __ballot_sync(0xffffffffu, bit);
-        mask &= bit ? bal : ~bal;
-    }
-    return mask;
-}
-
 __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdParams p) {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -315,8 +303,8 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
     const int64_t end = beg + wseg < cend ? beg + wseg : cend;
     for (uint32_t e = lane; e < E; e += 32) mine[e] = 0;
     __syncwarp();
-    // keys 0..E-1 are experts, E marks an out-of-range id
-    const int nbits = 32 - __clz(static_cast<int>(E));
+    // keys 0..E-1 are experts, E marks an out-of-range id; batches wholly
+    // past the segment's end are skipped (the same test for every lane)
 
     // pass 1: per-warp counts
     for (int64_t base = beg; base < end; base += 32 * kMapBatch) {
@@ -328,8 +316,9 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
         }
 #pragma unroll
         for (int b = 0; b < kMapBatch; ++b) {
+            if (base + b * 32 >= end) break;
             const uint32_t key = v[b] < E ? v[b] : E;
-            const unsigned grp = same_key_lanes(key, nbits);
+            const unsigned grp = __match_any_sync(0xffffffffu, key);
             if (key != E && lane == __ffs(grp) - 1) mine[key] += __popc(grp);
             __syncwarp();
         }
@@ -367,9 +356,10 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
         }
 #pragma unroll
         for (int b = 0; b < kMapBatch; ++b) {
+            if (base + b * 32 >= end) break;
             const int64_t r = base + b * 32 + lane;
             const uint32_t key = v[b] < E ? v[b] : E;
-            const unsigned grp = same_key_lanes(key, nbits);
+            const unsigned grp = __match_any_sync(0xffffffffu, key);
             if (key != E) {
                 const uint32_t pos = mine[key] + __popc(grp & lt_mask);
                 if (pos < static_cast<uint32_t>(p.m))

@@ -155,6 +155,24 @@ def test_tc_gemm_strides_offsets_broadcast(oracle_mod, dtype):
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
 
 
+# 160 tiles of 128 x 256: one full round on 152 SMs plus 8 tiles, which run as
+# 128-column half units; n = 1948 leaves 28 columns for the second half of
+# the last column block, n = 1892 none (that half unit computes nothing)
+LAST_ROUND_CASES = [
+    ("f16", False, True, 1948), ("bf16", False, True, 1892),
+    ("f16", False, False, 1948), ("bf16", True, True, 1892), ("f16", True, False, 1948),
+]
+
+
+@pytest.mark.parametrize("dtype,ta,tb,n", LAST_ROUND_CASES, ids=[str(c) for c in LAST_ROUND_CASES])
+def test_tc_gemm_last_round_half_units(oracle_mod, dtype, ta, tb, n):
+    m, k = 2560, 256
+    lda = _up8(m if ta else k)
+    ldb = _up8(k if tb else n)
+    g = StridedGemm(dtype, 1, m, n, k, ta, tb, lda=lda, ldb=ldb, std=1.0 / np.sqrt(k), seed=n + 3 * ta)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_tc_gemm_exact_small_integers(oracle_mod, dtype):
     # |v| <= 8 integers, k = 1024: every product and partial sum is an exact
