@@ -277,8 +277,15 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
                            s16(sa) && s16(sb) && m < (1LL << 31) && n < (1LL << 31) && k < (1LL << 31) &&
                            batch < (1LL << 31);
     if (tc_layout) {
-        const int bm = gemm_tc_block_m(), bn = gemm_tc_block_n(), bk = gemm_tc_block_k();
-        const int64_t tiles_m = (m + bm - 1) / bm, tiles_n = (n + bn - 1) / bn;
+        const int bn = gemm_tc_block_n(), bk = gemm_tc_block_k();
+        // 256-row tiles halve the operand bytes per MMA against 128-row tiles
+        // but keep no second accumulator for the epilogue to overlap with:
+        // taken for long k and at least two rounds of tiles over the SMs
+        const int wbm = gemm_tc_wide_block_m();
+        const int64_t tiles_n = (n + bn - 1) / bn;
+        const bool wide = k >= 512 && ((m + wbm - 1) / wbm) * tiles_n * batch >= 2LL * device_sm_count();
+        const int bm = wide ? wbm : gemm_tc_block_m();
+        const int64_t tiles_m = (m + bm - 1) / bm;
         const int64_t tiles = tiles_m * tiles_n * batch;
         const bool a_bc = sa == 0 || batch == 1, b_bc = sb == 0 || batch == 1;
         // A: [m, k] K-contiguous, or stored [k, m] when transposed; B: [n, k]
@@ -305,13 +312,16 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
             p.b_bcast = b_bc ? 1 : 0;
             p.a_mn = ta ? 1 : 0;
             p.b_mn = tb ? 0 : 1;
-            p.c_vec_ok = (a16(pc) && s16(ldc) && s16(sc)) ? 1 : 0;
+            // 1: rows 16-byte aligned; 2: 32-byte aligned
+            const bool c32 = reinterpret_cast<uintptr_t>(pc) % 32 == 0 && (ldc * 2) % 32 == 0 && (sc * 2) % 32 == 0;
+            p.c_vec_ok = (a16(pc) && s16(ldc) && s16(sc)) ? (c32 ? 2 : 1) : 0;
             p.tiles_m = static_cast<int32_t>(tiles_m);
             p.tiles_n = static_cast<int32_t>(tiles_n);
             p.num_tiles = static_cast<int32_t>(tiles);
             p.err = err;
             p.wait_limit_ns = kWaitLimitNs;
-            return after_launch(launch_gemm_tc(dt, map_a, map_b, p, device_sm_count(), stream),
+            return after_launch(wide ? launch_gemm_tc_wide(dt, map_a, map_b, p, device_sm_count(), stream)
+                                     : launch_gemm_tc(dt, map_a, map_b, p, device_sm_count(), stream),
                                 "gbmm_gemm_tc", stream);
         }
     }

@@ -69,7 +69,7 @@ struct GemmTcParams {
     int32_t m, n, k, batch;
     int32_t a_bcast, b_bcast;   // batch stride 0: always batch coordinate 0
     int32_t a_mn, b_mn;         // operand stored M- / N-contiguous
-    int32_t c_vec_ok;           // C rows allow 16-byte stores
+    int32_t c_vec_ok;           // C rows allow 16-byte stores (1) or 32-byte stores (2)
     int32_t tiles_m, tiles_n;
     int32_t num_tiles;
     uint32_t *err;
@@ -105,6 +105,10 @@ cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_small(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                            const GemmTcParams &p, int num_sms, cudaStream_t s);
+// 256 x 256 tiles (two 128-row sub-tiles sharing the B tile); A's tensor map
+// box is gemm_tc_wide_block_m() rows when A is K-contiguous
+cudaError_t launch_gemm_tc_wide(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                const GemmTcParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s);
@@ -115,6 +119,7 @@ int grouped_tc_max_experts();
 int grouped_tc_block_k();
 
 int gemm_tc_block_m();
+int gemm_tc_wide_block_m();
 int gemm_tc_block_n();
 int gemm_tc_block_k();
 int device_sm_count();

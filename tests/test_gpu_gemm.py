@@ -173,6 +173,33 @@ def test_tc_gemm_last_round_half_units(oracle_mod, dtype, ta, tb, n):
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
 
 
+# 256 x 256 tiles (k >= 512 and at least two rounds of them over the SMs):
+# 4 x 10 x 9 = 360 tiles with ragged m, n and k; the last round (56 tiles on
+# 152 SMs) runs as 128-row half units, and with m = 2404 the second half of
+# the last row block holds no rows.  Checked on sampled outputs: the corners
+# and edges of the sub-tiles, half units and ragged blocks, plus random ones.
+# ldc 2148 (rows 8-byte aligned: scalar stores), 2152 (16-byte), 2176 (32-byte)
+WIDE_CASES = [
+    ("f16", False, True, 2523, 2176), ("bf16", False, True, 2404, 2148), ("f16", False, False, 2404, 2152),
+    ("bf16", True, True, 2523, 2176), ("f16", True, False, 2523, 2148), ("bf16", True, False, 2404, 2176),
+]
+
+
+@pytest.mark.parametrize("dtype,ta,tb,m,ldc", WIDE_CASES, ids=[str(c) for c in WIDE_CASES])
+def test_tc_gemm_wide_tiles_sampled(oracle_mod, dtype, ta, tb, m, ldc):
+    batch, n, k = 4, 2148, 520
+    lda = _up8(m if ta else k)
+    ldb = _up8(k if tb else n)
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, lda=lda, ldb=ldb, ldc=ldc, std=1.0 / np.sqrt(k),
+                    seed=m + 5 * ta + tb)
+    rows = sorted({0, 127, 128, 255, 256, 2303, 2304, 2431, 2432, m - 1} - {r for r in range(m, 4096)})
+    cols = [0, 31, 255, 256, 2047, 2048, n - 1]
+    rng = np.random.default_rng(m + ta + 2 * tb)
+    idx = [bi * m * n + i * n + j for bi in range(batch) for i in rows for j in cols]
+    idx += list(rng.integers(0, batch * m * n, 6000))
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc", idx=np.array(idx, dtype=np.int64))
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_tc_gemm_exact_small_integers(oracle_mod, dtype):
     # |v| <= 8 integers, k = 1024: every product and partial sum is an exact
