@@ -218,6 +218,18 @@ def test_grouped_tc_tail_units(oracle_mod):
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
 
 
+@pytest.mark.parametrize("k", [40, 104, 136, 200, 264, 328, 448])
+def test_grouped_tc_k_block_orders(oracle_mod, k):
+    """1 to 7 k-blocks of 64 (ragged or whole), the short-k end of the
+    activation and weight rings.  9216 routed rows over 6 experts (about 12 row blocks each) x 3 column
+    blocks of n = 1300 (the last one cut past n): about 216 tiles, more than
+    CTAs, so the last round also runs as half units.  Every output."""
+    m, top_k, E = 3072, 3, 6
+    case = synth.matmul_id_case(f"korder-{k}", "bf16", m, 1300, k, top_k, E, route=1, seed=k)
+    Run(case).call().check(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+
+
 @pytest.mark.parametrize("route", [0, 1])
 def test_out_of_range_ids_give_zero_rows(oracle_mod, route):
     m, top_k, E = 40, 4, 9
