@@ -305,12 +305,16 @@ def run_ours(args) -> None:
     sptr = int(stream.cuda_stream)
     n_launch = sum(p.launches for p in probs.values())
 
-    def step(events=None):
+    def step(events=None, around=None):
+        # events[i] before call i and events[-1] after the last one; with
+        # `around`, only events[0] / events[1] around that call
         for i, k in enumerate(keys):
-            if events is not None:
-                events[i].record(stream)
+            if events is not None and (around is None or k == around):
+                events[0 if around else i].record(stream)
             probs[k].call(sptr)
-        if events is not None:
+            if events is not None and k == around:
+                events[1].record(stream)
+        if events is not None and around is None:
             events[len(keys)].record(stream)
 
     torch.cuda.synchronize()
@@ -318,10 +322,21 @@ def run_ours(args) -> None:
         step()
     torch.cuda.synchronize()
 
-    # per-call durations from events between the launches of each step
-    per_call = {k: 0.0 for k in keys}
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(keys) + 1)]
-          for _ in range(args.steps)]
+    # per-call split: an instrumented pass with an event between every two
+    # launches (each event costs a few microseconds of the step, so the
+    # timed steps below carry events around the dominant call only)
+    split_steps = max(3, min(args.steps, 10))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(keys) + 1)] for _ in range(split_steps)]
+    for s in range(split_steps):
+        step(ev[s])
+    torch.cuda.synchronize()
+    per_call = {k: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(split_steps)) / split_steps
+                for i, k in enumerate(keys)}
+    dom = max(keys, key=lambda k: per_call[k])
+
+    # the timed steps: the whole hot path back to back, the dominant call's
+    # launches bracketed by events on the launching stream
+    dev_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
@@ -333,7 +348,7 @@ def run_ours(args) -> None:
     t_wall = time.perf_counter()
     start.record(stream)
     for s in range(args.steps):
-        step(ev[s])
+        step(dev_ev[s], around=dom)
     end.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
@@ -343,10 +358,9 @@ def run_ours(args) -> None:
     time.sleep(0.1)
     clk = clocks.stop()
     elapsed_ms = start.elapsed_time(end)
-    for s in range(args.steps):
-        for i, k in enumerate(keys):
-            per_call[k] += ev[s][i].elapsed_time(ev[s][i + 1])
-    per_call = {k: v / args.steps for k, v in per_call.items()}
+    dom_ms_live = sum(e[0].elapsed_time(e[1]) for e in dev_ev) / args.steps
+    per_call_split = dict(per_call)
+    per_call[dom] = dom_ms_live
 
     elapsed_ms = max_over_ranks(elapsed_ms, device="cuda")
     ms_per_step = elapsed_ms / args.steps
@@ -477,7 +491,6 @@ def run_ours(args) -> None:
         if "distinct_experts" in wk:
             entry["distinct_experts"] = wk["distinct_experts"]
         calls[k] = entry
-    dom = max(keys, key=lambda k: per_call[k])
     wk = works[dom]
     secs = per_call[dom] / 1e3
     if wk["bound"] in ("tensor",):
@@ -510,6 +523,11 @@ def run_ours(args) -> None:
                                                                     "bf16_tflops_sustained")
                                                                    if k in peaks},
                    "roofline_ms_per_step": roof_total * 1e3, "calls": calls,
+                   "calls_timing": (f"{dom}: events around its launches in every timed step; the other "
+                                    f"calls: an instrumented pass of {split_steps} steps with an event "
+                                    "between every two launches (those events are kept out of the timed "
+                                    "steps)"),
+                   "calls_split_ms": per_call_split,
                    "c5_single_rounding_option": single},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk, "wall_s_timed": wall,
