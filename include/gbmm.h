@@ -17,6 +17,11 @@
  *     nothing.  gbmm_last_error() then describes the failure.
  *   - Thread safety: calls may be made from several host threads; the error
  *     string is per thread.
+ *   - Debugging: with the environment variable GBMM_DEBUG_SYNC=1 (read once
+ *     per process) every launch is followed by a stream synchronisation, so a
+ *     kernel that fails on the device is reported by the call that launched
+ *     it (GBMM_ERR_CUDA, with the kernel's name in gbmm_last_error()) -- the
+ *     counterpart of [P1]'s debug wait_until_completed.
  *
  * Sources (page titles and the items on them)
  *   [P1] tract-metal 0.23.6, src/kernels/matmul/mlx_gemm/mod.rs
