@@ -314,3 +314,55 @@ def test_grouped_single_rounding_mode(oracle_mod, layout):
     assert np.all(np.abs(got - ref) <= (2.0 ** -8 + 1e-5) * ref_abs)
     assert_close(got, ref, ref_abs, "bf16", "f32", "single-rounding mode, zero-mean data")
     r.check_map(oracle_mod)
+
+
+# ---------------------------------------------------------------------------
+# degenerate and maximum cases
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("route", [0, 1])
+def test_single_expert_is_a_plain_gemm(oracle_mod, route):
+    """n_experts = 1, top_k = 1, every id 0: out[t, 0, :] = W_0 x_t, the dense
+    GEMM x [m, k] times W_0 stored [n, k] -- checked against the oracle's
+    expert-ID loop and against its separate dense GEMM loop."""
+    m, n, k = 70, 300, 264
+    ids = np.zeros((m, 1), dtype=np.uint32)
+    case = synth.matmul_id_case("one", "bf16", m, n, k, 1, 1, route=route, ids=ids)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    w32 = synth.bf16_bits_to_f32(case.w)[: n * k]
+    ref, ref_abs = oracle_mod.gemm("f32", 1, m, n, k, False, True, case.x.reshape(-1), k, m * k, w32, k, n * k)
+    assert_close(r.output().reshape(m, n), ref.reshape(m, n), ref_abs.reshape(m, n), "bf16", "f32", "E=1 as GEMM")
+
+
+@pytest.mark.parametrize("route", [0, 1])
+def test_no_id_in_range(oracle_mod, route):
+    """No id selects an expert (all equal to n_experts or above): every output
+    row is zero and, on the grouped route, every expert count is zero."""
+    m, top_k, E = 33, 3, 5
+    ids = np.full((m, top_k), E, dtype=np.uint32)
+    ids[::2, 1] = 0xFFFFFFFF
+    ids[1::3, 2] = E + 7
+    case = synth.matmul_id_case("none", "bf16", m, 136, 64, top_k, E, route=route, ids=ids)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    assert np.all(r.output() == 0.0)
+    if route == 1:
+        assert np.all(r.counts.read(np.uint32, E) == 0)
+
+
+def test_grouped_max_experts(oracle_mod):
+    """n_experts = 1024, the grouped route's limit: 1200 routed rows over 1024
+    experts (most lists hold 0 to 3 rows).  Every output and the map."""
+    m, top_k, E = 300, 4, 1024
+    case = synth.matmul_id_case("e1024", "bf16", m, 264, 136, top_k, E, route=1, seed=5)
+    Run(case).call().check(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+
+
+@pytest.mark.parametrize("route", [0, 1])
+def test_single_token_and_every_expert(oracle_mod, route):
+    """One token (m = 1), and top_k = n_experts (every token picks every
+    expert, in a per-token permuted order)."""
+    Run(synth.matmul_id_case("m1", "bf16", 1, 300, 200, 8, 16, route=route, seed=4)).call().check(oracle_mod)
+    Run(synth.matmul_id_case("all", "bf16", 40, 136, 264, 6, 6, route=route, seed=6)).call().check(oracle_mod)
