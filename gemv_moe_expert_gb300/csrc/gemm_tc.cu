@@ -9,7 +9,11 @@
 // `dispatch_metal_mlx_gemm` (B stored [n, k] when transposed; batch strides
 // per operand) and rlx-metal 0.2.14, src/mps_blas.rs (transposeRight).
 //
-// Design (one persistent CTA per SM, 6 warps, warp-specialised):
+// Two kernels: gemm_tc_wide_kernel (256 x 256 tiles, see its section below)
+// for long-k problems with at least two rounds of such tiles, and
+// gemm_tc_kernel (128 x 256 tiles) for the rest; the host picks one.
+//
+// Design of gemm_tc_kernel (one persistent CTA per SM, 6 warps, warp-specialised):
 //   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles, 128-byte
 //               swizzled, into a 4-stage shared-memory ring (48 KB/stage);
 //               a K-major tile is one box of 64 k x 128 / 256 rows, an
