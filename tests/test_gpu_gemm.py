@@ -200,6 +200,21 @@ def test_tc_gemm_wide_tiles_sampled(oracle_mod, dtype, ta, tb, m, ldc):
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc", idx=np.array(idx, dtype=np.int64))
 
 
+@pytest.mark.parametrize("dtype,ta,tb,bcast", [("f16", False, True, "a"), ("bf16", True, False, "b")])
+def test_tc_gemm_wide_tiles_broadcast_sampled(oracle_mod, dtype, ta, tb, bcast):
+    """256 x 256 tiles (4 x 10 x 8 = 320 of them) with one operand shared by
+    every batch (batch stride 0).  Sampled outputs of every batch."""
+    batch, m, n, k = 4, 2560, 2048, 520
+    lda = _up8(m if ta else k)
+    ldb = _up8(k if tb else n)
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, lda=lda, ldb=ldb, sa=0 if bcast == "a" else None,
+                    sb=0 if bcast == "b" else None, std=1.0 / np.sqrt(k), seed=7 + ta)
+    rng = np.random.default_rng(17)
+    idx = [bi * m * n + i * n + j for bi in range(batch) for i in (0, 255, 256, m - 1) for j in (0, 255, 256, n - 1)]
+    idx += list(rng.integers(0, batch * m * n, 4000))
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc", idx=np.array(idx, dtype=np.int64))
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_tc_gemm_exact_small_integers(oracle_mod, dtype):
     # |v| <= 8 integers, k = 1024: every product and partial sum is an exact
