@@ -659,6 +659,122 @@ def run_crossover(args) -> None:
                       "grouped_faster_from_m": cross}), flush=True)
 
 
+def _time_alone(call, torch, flush, steps, warmup):
+    """Median of `steps` calls, each timed with CUDA events after an L2 flush.
+    A device-side spin (about 0.2 ms) is queued between the flush and the start
+    event so that the host has enqueued the call before the GPU reaches the
+    event: the interval holds the call's device time, not the host's argument
+    marshalling and launch latency."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.fill_(1)
+        torch.cuda._sleep(400_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+def run_skinny(args) -> None:
+    """The decode GEMV y[m, n] = x[m, k] W[n, k]^T (B stored [n, k], batch 1)
+    for m = 1 .. 15 tokens on the decode workload's shape (n 11008, k 4096), f16
+    and bf16 (and f32 at m = 1): each call timed alone after an L2 flush, with
+    the kernel that served it and its fraction of the HBM roofline (bytes of W,
+    x and y)."""
+    import torch
+    from gemv_moe_expert_gb300 import binding as gb
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+    peaks, _ = load_peaks()
+    n, k = 11008, 4096
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rows = []
+    for dt, tdt, ms in (("f16", torch.float16, (1, 2, 3, 4, 6, 8, 12, 15)),
+                        ("bf16", torch.bfloat16, (1, 2, 4, 8, 15)), ("f32", torch.float32, (1,))):
+        size = synth.ITEMSIZE[dt]
+        w = (torch.randn(n * k, device="cuda", generator=g) * 0.02).to(tdt)
+        for m in ms:
+            x = torch.randn(m * k, device="cuda", generator=g).to(tdt)
+            y = torch.empty(m * n, device="cuda", dtype=tdt)
+
+            def call():
+                gb.check(gb.gbmm_gemm(dt, 1, m, n, k, 0, 1, x, 0, k, m * k, w, 0, k, n * k, y, 0, n, m * n))
+            us = _time_alone(call, torch, flush, args.steps, args.warmup)
+            bytes_ = (n * k + m * k + m * n) * size
+            rows.append({"dtype": dt, "m": m, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
+                         "frac_of_hbm": bytes_ / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6),
+                         "kernel": gb.gbmm_test_last_kernel()})
+    print(json.dumps({"sweep": "skinny decode GEMV", "n": n, "k": k, "layout": "B stored [n, k], batch 1",
+                      "timing": "each call alone after an L2 flush, median of --steps", "rows": rows}), flush=True)
+
+
+def run_dtypes(args) -> None:
+    """The expert-ID matmul for every weight dtype, input layout and id
+    multiplicity the capability accepts: Direct on a decode shape (4 tokens x
+    top-8 of 64 experts, k 2048, n 1408) and GroupedPrefill on a prefill shape
+    (512 tokens, same experts), each call timed alone after an L2 flush, with
+    its fraction of the roofline (HBM bytes of the experts the call reads, x,
+    ids and out; tensor flops at the bf16 peak for 16-bit weights, the FFMA
+    peak for f32 weights)."""
+    import torch
+    from gemv_moe_expert_gb300 import binding as gb
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+    peaks, _ = load_peaks()
+    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    E, top_k, k, n = 64, 8, 2048, 1408
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rows = []
+    for wdt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16), ("f32", torch.float32)):
+        size = synth.ITEMSIZE[wdt]
+        w = (torch.randn(E * n * k, device="cuda", generator=g) * 0.02).to(tdt)
+        cases = [("direct", 4, 0, 0), ("direct", 4, 1, 0), ("direct", 4, 0, 1),
+                 ("grouped", 512, 0, 0), ("grouped", 512, 1, 0)]
+        for route_name, m, layout, mult in cases:
+            route = gb.ROUTE_DIRECT if route_name == "direct" else gb.ROUTE_GROUPED_PREFILL
+            ids_h = (synth.repeat_ids(m, top_k, E, seed=m) if mult else synth.distinct_ids(m, top_k, E, seed=m))
+            ids = torch.from_numpy(ids_h.view(np.int32).reshape(-1).copy()).cuda()
+            x_rows = m if layout == 0 else m * top_k
+            x = torch.randn(x_rows * k, device="cuda", generator=g)
+            out = torch.empty(m * top_k * n, device="cuda")
+            p = gb.make_params(m, n, k, top_k, E, n * k * size, layout, mult, route)
+            st, cap = gb.gbmm_matmul_id_capability(wdt, p)
+            gb.check(st)
+            sc = None
+            if route == gb.ROUTE_GROUPED_PREFILL:
+                cnt = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device="cuda")
+                rr = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device="cuda")
+                sc = gb.make_scratch(cnt, cap.expert_counts_bytes, rr, cap.routed_rows_bytes, E, m)
+
+            def call():
+                gb.check(gb.gbmm_matmul_id(p, wdt, w, w.numel() * size, x, x.numel() * 4, ids, ids.numel() * 4,
+                                           out, out.numel() * 4, sc)[0])
+            us = _time_alone(call, torch, flush, args.steps, args.warmup)
+            distinct = int(len(np.unique(ids_h)))
+            bytes_ = distinct * n * k * size + x.numel() * 4 + ids.numel() * 4 + out.numel() * 4
+            flops = 2 * m * top_k * n * k
+            peak_tf = ffma_peak_tflops() if wdt == "f32" else tensor_peak
+            roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12))
+            rows.append({"weights": wdt, "route": route_name, "m": m,
+                         "layout": "Slotted" if layout else "SharedPerToken",
+                         "ids": "MayRepeat" if mult else "DistinctPerToken", "distinct_experts": distinct,
+                         "us": us, "roofline_us": roof * 1e6, "frac_of_roofline": roof / (us * 1e-6),
+                         "kernel": gb.gbmm_test_last_kernel()})
+    print(json.dumps({"sweep": "matmul_id weight dtypes, layouts and multiplicity", "experts": E,
+                      "top_k": top_k, "k": k, "n": n, "timing": "each call alone after an L2 flush, median of --steps",
+                      "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -670,14 +786,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-scale", type=float, default=1.0)
     ap.add_argument("--no-options", action="store_true", help="skip the opt-in mode side timings")
-    ap.add_argument("--sweep", choices=["crossover"], default=None,
-                    help="instead of the step: time Direct against GroupedPrefill for m = 1..512")
+    ap.add_argument("--sweep", choices=["crossover", "skinny", "dtypes"], default=None,
+                    help="instead of the step: crossover = Direct against GroupedPrefill for m = 1..512; "
+                         "skinny = the decode GEMV for m = 1..15; dtypes = the expert-ID matmul for every "
+                         "weight dtype, input layout and id multiplicity")
     args = ap.parse_args()
     args.only = [k.strip() for k in args.only.split(",") if k.strip()]
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.sweep == "crossover":
         run_crossover(args)
+    elif args.sweep == "skinny":
+        run_skinny(args)
+    elif args.sweep == "dtypes":
+        run_dtypes(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

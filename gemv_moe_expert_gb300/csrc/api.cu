@@ -214,6 +214,28 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
     // ---- skinny / wide: a few rows of A against B stored [n, k] ----
     const bool wide = !gemv_only && dt != GBMM_F32 && !ta && tb && batch == 1 && m >= 2 && m <= 15 &&
                       n > 1;
+    // the skinny case on the tensor cores: y^T = W x^T, the weight rows as the
+    // MMA's M side and the (up to 15) tokens as its N side
+    if (wide && a16(pa) && a16(pb) && s16(lda) && s16(ldb) && k < (1LL << 31) && n < (1LL << 31) &&
+        gemv_tc_block_k() == 64) {
+        CUtensorMap map_w, map_x;
+        if (encode_operand(&map_w, dt, pb, k, n, 1, ldb, sb, true, static_cast<uint32_t>(gemv_tc_block_rows())) &&
+            encode_operand(&map_x, dt, pa, k, m, 1, lda, sa, true, static_cast<uint32_t>(gemv_tc_max_tokens()))) {
+            if (!resolve("gbmm_gemv_tc")) return GBMM_ERR_KERNEL_UNAVAILABLE;
+            uint32_t *err = device_error_word();
+            if (err == nullptr) return fail(GBMM_ERR_CUDA, "%s: device error word unavailable", fn);
+            GemvTcParams tp{};
+            tp.c = pc;
+            tp.ldc = ldc;
+            tp.m = static_cast<int32_t>(m);
+            tp.n = static_cast<int32_t>(n);
+            tp.k = static_cast<int32_t>(k);
+            tp.ksplit = gemv_tc_split(n, k, device_sm_count());
+            tp.err = err;
+            tp.wait_limit_ns = kWaitLimitNs;
+            return after_launch(launch_gemv_tc(dt, map_w, map_x, tp, stream), "gbmm_gemv_tc", stream);
+        }
+    }
     if (wide || m == 1 || n == 1) {
         GemvParams g{};
         g.k = k;

@@ -23,6 +23,7 @@ enum KernelId : uint32_t {
     kKidGroupedTc = 2,
     kKidBoundedWaitTest = 3,
     kKidGemvStream = 4,
+    kKidGemvTc = 5,
 };
 
 // default limit of a bounded device wait (1 s)
@@ -92,6 +93,17 @@ struct MatmulIdParams {
     uint64_t wait_limit_ns;
 };
 
+// Skinny decode GEMV on the tensor cores: y[m, n] (row stride ldc) =
+// x[m, k] W[n, k]^T, the operands read through tensor maps.
+struct GemvTcParams {
+    void *c;
+    int64_t ldc;
+    int32_t m, n, k;
+    int32_t ksplit;  // CTAs per cluster splitting k (1..8), from gemv_tc_split()
+    uint32_t *err;
+    uint64_t wait_limit_ns;
+};
+
 // ---- launchers (each returns the launch's cudaError_t) --------------------
 
 cudaError_t launch_fill_zero(int dt, void *c, int64_t batch, int64_t m, int64_t n, int64_t ldc,
@@ -101,6 +113,15 @@ cudaError_t launch_gemv_coldot(int dt, const GemvParams &p, cudaStream_t s);
 // staged-stream GEMV (stream.cu) and the shapes it takes
 bool gemv_stream_eligible(int dt, const GemvParams &p);
 cudaError_t launch_gemv_stream(int dt, const GemvParams &p, int num_sms, cudaStream_t s);
+// skinny decode GEMV on the tensor cores (gemv_tc.cu): W boxes of
+// gemv_tc_block_rows() rows, x boxes of gemv_tc_max_tokens() rows, both
+// gemv_tc_block_k() wide
+cudaError_t launch_gemv_tc(int dt, const CUtensorMap &map_w, const CUtensorMap &map_x, const GemvTcParams &p,
+                           cudaStream_t s);
+int gemv_tc_block_rows();
+int gemv_tc_max_tokens();
+int gemv_tc_block_k();
+int gemv_tc_split(int64_t n, int64_t k, int num_sms);
 cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_small(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,

@@ -353,7 +353,7 @@ GBMM_API gbmm_status gbmm_device_error(gbmm_stream stream, uint32_t *code);
 
 /* Makes the next resolution of kernel `name` fail (one shot), like [P2]'s
  * `KernelRegistry::inject_next_pipeline_lookup_failure`.  NULL clears it.
- * Kernel names: "gbmm_gemv_rowdot", "gbmm_gemv_coldot", "gbmm_gemm_simt",
+ * Kernel names: "gbmm_gemv_rowdot", "gbmm_gemv_coldot", "gbmm_gemv_tc", "gbmm_gemm_simt",
  * "gbmm_gemm_tc", "gbmm_fill_zero", "gbmm_matmul_id_direct",
  * "gbmm_matmul_id_map", "gbmm_matmul_id_grouped". */
 GBMM_API void gbmm_test_inject_kernel_failure(const char *name);

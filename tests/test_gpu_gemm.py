@@ -312,12 +312,16 @@ STREAM_CASES = [
     ("f16", 1000, 4096, None, 1, "gbmm_gemv_stream"),     # two 8 KB rows per slot
     ("f32", 301, 4096, None, 1, "gbmm_gemv_stream"),      # one 16 KB row per slot
     ("bf16", 777, 1000, None, 1, "gbmm_gemv_stream"),     # eight 2000-byte rows per slot, ragged tail
-    ("bf16", 515, 1024, 1032, 3, "gbmm_gemv_stream"),     # padded rows (ldb > k): one copy per row
-    ("f16", 129, 6000, 6008, 2, "gbmm_gemv_stream"),      # padded, one 12000-byte row per slot
+    ("f32", 515, 1024, 1032, 1, "gbmm_gemv_stream"),      # padded rows (ldb > k): one copy per row
+    ("f16", 129, 6000, 6008, 1, "gbmm_gemv_stream"),      # padded, one 12000-byte row per slot
     ("f32", 64, 16, None, 1, "gbmm_gemv_stream"),         # 64-byte rows, 256 per slot
-    ("f16", 5, 8, None, 7, "gbmm_gemv_stream"),           # fewer rows than CTAs
+    ("f16", 5, 8, None, 1, "gbmm_gemv_stream"),           # fewer rows than CTAs
     ("f32", 301, 5000, None, 1, "gbmm_gemv_rowdot"),      # 20000-byte rows
-    ("f16", 129, 12000, None, 2, "gbmm_gemv_rowdot"),     # 24000-byte rows
+    ("f16", 129, 12000, None, 1, "gbmm_gemv_rowdot"),     # 24000-byte rows
+    # several tokens (2..15, 16-bit, B stored [n, k]): the tensor-core skinny kernel
+    ("bf16", 515, 1024, 1032, 3, "gbmm_gemv_tc"),         # padded weight rows
+    ("f16", 129, 6000, 6008, 2, "gbmm_gemv_tc"),          # ragged k-block, padded rows
+    ("f16", 5, 8, None, 7, "gbmm_gemv_tc"),               # k = 8: one partial k-block
 ]
 
 
@@ -353,15 +357,44 @@ def test_wide_skinny_ramp(oracle_mod, dtype, m, n, k):
     g.b[:] = synth.ramp((n * k,), 2, dtype)
     run_case(oracle_mod, g)
     if dtype != "f32":
-        assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_rowdot", "gbmm_gemv_stream")
+        assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_rowdot", "gbmm_gemv_stream", "gbmm_gemv_tc")
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("m", list(range(2, 16)))
 def test_wide_skinny_random(oracle_mod, dtype, m):
+    # 16-byte multiples for every row stride: the tensor-core skinny kernel (ragged n
+    # and k: the last weight tile and k-block are partly outside the operands)
     g = StridedGemm(dtype, 1, m, 256 + 3, 4096 + 8, False, True, lda=4096 + 16, ldc=300, seed=m)
-    # m vectors of 8208 bytes are staged in 64 KB of shared memory up to m = 7
-    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_stream" if m <= 7 else "gbmm_gemv_rowdot")
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_tc")
+    # a row stride that is not a multiple of 16 bytes: the CUDA-core kernels
+    g = StridedGemm(dtype, 1, m, 256 + 3, 4096 + 8, False, True, lda=4096 + 13, ldc=300, seed=m + 1)
+    run_case(oracle_mod, g)
+    assert gb.gbmm_test_last_kernel() in ("gbmm_gemv_stream", "gbmm_gemv_rowdot")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("m,n", [(2, 11008), (7, 11008), (15, 11008), (15, 1037)])
+def test_skinny_tensor_core_decode_shape(oracle_mod, dtype, m, n):
+    """y = x W^T for 2..15 tokens on the decode GEMV's weight shape (k 4096),
+    and a ragged n; every output against the oracle."""
+    k = 4096
+    g = StridedGemm(dtype, 1, m, n, k, False, True, std=1.0 / np.sqrt(k), seed=m + n)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_tc")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_skinny_tensor_core_exact_small_integers(oracle_mod, dtype):
+    """|v| <= 8 integers, k = 1024: every partial sum is exact in f32, so the
+    output equals the oracle's value rounded once to the output dtype."""
+    g = StridedGemm(dtype, 1, 11, 700, 1024, False, True, dist="ints", seed=3)
+    a, b, c = g.device()
+    assert gb.gbmm_gemm(*g.args(a, b, c)) == gb.GBMM_OK
+    assert gb.gbmm_test_last_kernel() == "gbmm_gemv_tc"
+    got = g.gather_c(c)
+    ref, _ = g.oracle(oracle_mod)
+    rounded = to_f64(synth._store(ref.astype(np.float32).reshape(-1), dtype), dtype).reshape(ref.shape)
+    assert np.array_equal(got, rounded)
 
 
 # ---------------------------------------------------------------------------
