@@ -1,9 +1,10 @@
-// stream.cu -- the HBM-bound row-dot matrix x vector as a staged stream
-// (m == 1, and the skinny "wide" case of up to 16 vectors).
+// stream.cu -- the HBM-bound row-dot matrix x vector (m == 1, or n == 1
+// with A stored row-major) as a staged stream.
 //
 // Semantics: tract-metal 0.23.6, src/kernels/matmul/mlx_gemm/mod.rs,
-// `dispatch_metal_mlx_gemv` / `dispatch_metal_mlx_gemv_wide` (each output is
-// a dot product along a contiguous matrix row).
+// `dispatch_metal_mlx_gemv` (each output is a dot product along a contiguous
+// matrix row).  Two to fifteen vectors (the skinny case) go to the tensor
+// cores instead (gemv_tc.cu).
 //
 // Every matrix byte is read exactly once, so the kernel runs at the speed
 // HBM delivers bytes to the SMs.  A kernel that keeps loads in
@@ -19,8 +20,8 @@
 //     needed for an SM's share of HBM bandwidth (4 KB copies reach a third
 //     of it); padded rows are copied one per producer lane in parallel;
 //   * the consumer warps take the staged rows round-robin (row slot t of the
-//     CTA goes to warp t mod 8), dot each with the vectors (staged once per
-//     CTA in shared memory) using several independent partial sums, reduce
+//     CTA goes to warp t mod 8), dot each with the vector (staged once per
+//     CTA in shared memory) using four independent partial sums, reduce
 //     across the warp with shuffles and write the outputs; a slot is free
 //     again once every one of its row slots was released.
 // Every wait is bounded: on timeout the kernel raises its abort flag and the
@@ -35,7 +36,7 @@ constexpr int kGemvWarps = 8;     // consumer warps
 constexpr int kSlots = 8;
 constexpr uint32_t kSlotBytes = 16384;
 constexpr uint32_t kRingBytes = kSlots * kSlotBytes;
-constexpr uint32_t kStageXMax = 65536;        // vector bytes staged per CTA
+constexpr uint32_t kStageXMax = kSlotBytes;   // vector bytes staged per CTA: one row
 
 // shared-memory layout after the ring (byte offsets from the 1024-aligned base)
 constexpr uint32_t kBarOff = kRingBytes;                      // full[kSlots], empty[kSlots]
@@ -217,13 +218,13 @@ struct RowCursor {
 //
 // Pieces: groups of rp = kSlotBytes / row bytes consecutive rows, one per
 // slot fill; CTA b streams its balanced share of the pieces.  Each dot
-// product keeps kAcc independent partial sums per vector, so the FMA chain
-// latency is hidden with only two consumer warps per scheduler.
-template <typename T, int NV>
+// product keeps kAcc independent partial sums, so the FMA chain latency is
+// hidden with only two consumer warps per scheduler.
+template <typename T>
 __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) gemv_stream_kernel(GemvParams p, int rp) {
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = kGemvWarps;
-    constexpr int kAcc = NV == 1 ? 4 : (NV == 2 ? 2 : 1);
+    constexpr int kAcc = 4;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -261,13 +262,13 @@ __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) gemv_stream_kernel(G
         }
     } else {
         // ---------------- consumers ----------------
-        // the vectors: chunk c of vector r at xs[r * nch + c]
+        // the vector: chunk c at xs[c]
         const T *vec = static_cast<const T *>(p.vec);
         const int64_t nch = row_bytes / 16;
         const uint4 *xs = reinterpret_cast<const uint4 *>(smem + kXOff);
-        stage16(reinterpret_cast<uint4 *>(smem + kXOff), nch * p.nvec,
-                [&](int64_t c) { return static_cast<const void *>(vec + (c / nch) * p.vec_rr + (c % nch) * V); },
-                [](int64_t c) { return c; }, threadIdx.x, NW * 32);
+        stage16(reinterpret_cast<uint4 *>(smem + kXOff), nch,
+                [&](int64_t c) { return static_cast<const void *>(vec + c * V); }, [](int64_t c) { return c; },
+                threadIdx.x, NW * 32);
         consumers_sync<NW>();
 
         T *out = static_cast<T *>(p.out);
@@ -282,33 +283,22 @@ __global__ void __launch_bounds__((kGemvWarps + 1) * 32, 1) gemv_stream_kernel(G
             if (row < p.rows) {
                 const uint4 *wr = reinterpret_cast<const uint4 *>(smem + (i % kSlots) * kSlotBytes +
                                                                   static_cast<uint32_t>(rc.q) * row_bytes);
-                float acc[NV][kAcc];
+                float acc[kAcc];
 #pragma unroll
-                for (int r = 0; r < NV; ++r)
-#pragma unroll
-                    for (int a = 0; a < kAcc; ++a) acc[r][a] = 0.f;
+                for (int a = 0; a < kAcc; ++a) acc[a] = 0.f;
 #pragma unroll 2
                 for (int c = lane; c < nc; c += 32) {
-                    float wf[V];
+                    float wf[V], xf[V];
                     unpack16<T>(wr[c], wf);
+                    unpack16<T>(xs[c], xf);
 #pragma unroll
-                    for (int r = 0; r < NV; ++r) {
-                        if (NV == 1 || r < p.nvec) {
-                            float xf[V];
-                            unpack16<T>(xs[r * nch + c], xf);
-#pragma unroll
-                            for (int e = 0; e < V; ++e) acc[r][e % kAcc] = fmaf(wf[e], xf[e], acc[r][e % kAcc]);
-                        }
-                    }
+                    for (int e = 0; e < V; ++e) acc[e % kAcc] = fmaf(wf[e], xf[e], acc[e % kAcc]);
                 }
+                float v = acc[0];
 #pragma unroll
-                for (int r = 0; r < NV; ++r) {
-                    float v = acc[r][0];
-#pragma unroll
-                    for (int a = 1; a < kAcc; ++a) v += acc[r][a];
-                    v = warp_sum(v);
-                    if (lane == 0 && (NV == 1 || r < p.nvec)) out[r * p.out_rr + row * p.out_os] = Elem<T>::from_f(v);
-                }
+                for (int a = 1; a < kAcc; ++a) v += acc[a];
+                v = warp_sum(v);
+                if (lane == 0) out[row * p.out_os] = Elem<T>::from_f(v);
             }
             ring_release(ring, i, lane);
         }
@@ -329,35 +319,25 @@ cudaError_t set_smem_once(K kernel, uint32_t bytes, unsigned long long &done) {
     return e;
 }
 
-template <typename T, int NV>
-cudaError_t gemv_stream_nv(const GemvParams &p, int num_sms, cudaStream_t s) {
+template <typename T>
+cudaError_t gemv_stream_t(const GemvParams &p, int num_sms, cudaStream_t s) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.k * sizeof(T));
     const int rp = static_cast<int>(kSlotBytes / row_bytes);
     const int64_t pieces = (p.rows + rp - 1) / rp;
     const int64_t grid = pieces < num_sms ? pieces : num_sms;
     static unsigned long long done = 0;
-    cudaError_t e = set_smem_once(gemv_stream_kernel<T, NV>, kStreamSmem, done);
+    cudaError_t e = set_smem_once(gemv_stream_kernel<T>, kStreamSmem, done);
     if (e != cudaSuccess) return e;
-    gemv_stream_kernel<T, NV><<<static_cast<unsigned>(grid), (kGemvWarps + 1) * 32, kStreamSmem, s>>>(p, rp);
+    gemv_stream_kernel<T><<<static_cast<unsigned>(grid), (kGemvWarps + 1) * 32, kStreamSmem, s>>>(p, rp);
     return cudaGetLastError();
-}
-
-template <typename T>
-cudaError_t gemv_stream_t(const GemvParams &p, int num_sms, cudaStream_t s) {
-    if (p.nvec <= 1) return gemv_stream_nv<T, 1>(p, num_sms, s);
-    if (p.nvec <= 2) return gemv_stream_nv<T, 2>(p, num_sms, s);
-    if (p.nvec <= 4) return gemv_stream_nv<T, 4>(p, num_sms, s);
-    if (p.nvec <= 8) return gemv_stream_nv<T, 8>(p, num_sms, s);
-    return gemv_stream_nv<T, 16>(p, num_sms, s);
 }
 
 }  // namespace
 
 bool gemv_stream_eligible(int dt, const GemvParams &p) {
     const int64_t size = dtype_size(dt);
-    return p.vec_ok && p.batch == 1 && p.mat_ks == 1 && p.vec_ks == 1 && p.nvec >= 1 && p.nvec <= 16 &&
-           (p.k * size) % 16 == 0 && p.k * size <= static_cast<int64_t>(kSlotBytes) &&
-           p.k * size * p.nvec <= static_cast<int64_t>(kStageXMax);
+    return p.vec_ok && p.batch == 1 && p.mat_ks == 1 && p.vec_ks == 1 && p.nvec == 1 &&
+           (p.k * size) % 16 == 0 && p.k * size <= static_cast<int64_t>(kSlotBytes);
 }
 
 cudaError_t launch_gemv_stream(int dt, const GemvParams &p, int num_sms, cudaStream_t s) {
