@@ -28,6 +28,8 @@
 // the same launch zero-fill output rows whose id is out of range.
 #include <cooperative_groups.h>
 
+#include <type_traits>
+
 #include "device_common.cuh"
 
 namespace cg = cooperative_groups;
@@ -375,15 +377,27 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
 // ---------------------------------------------------------------------------
 // grouped GEMM on the FFMA pipe (any weight dtype)
 // ---------------------------------------------------------------------------
+//
+// One CTA per (128 routed rows of expert e, 128 outputs): the rows are
+// gathered through routed_rows, the weights widened to f32 as they land in
+// shared memory.  256 threads, each an 8 x 8 block of outputs (rows
+// {4 ty .. 4 ty + 3, 64 + 4 ty ..}, columns likewise with tx), so every
+// 16-wide k step reads four 16-byte shared-memory vectors per 64 FMAs.  The
+// next k step's tiles are loaded into registers while the current one is
+// multiplied (two shared-memory buffers, one barrier per step).
 
-constexpr int kGM = 64;
-constexpr int kGN = 64;
+constexpr int kGM = 128;
+constexpr int kGN = 128;
 constexpr int kGK = 16;
+constexpr int kGThreads = 256;
+constexpr int kGPitch = kGM + 4;  // keeps 16-byte alignment of each k row
 
 template <typename TW>
-__global__ void __launch_bounds__(256) matmul_id_grouped_simt_kernel(MatmulIdParams p) {
-    __shared__ float As[kGK][kGM + 4];
-    __shared__ float Bs[kGK][kGN + 4];
+__global__ void __launch_bounds__(kGThreads, 2) matmul_id_grouped_simt_kernel(MatmulIdParams p, int vec_ok,
+                                                                               int out_vec_ok) {
+    constexpr int kV = 16 / static_cast<int>(sizeof(TW));  // weight elements per 16-byte vector
+    __shared__ __align__(16) float As[2][kGK][kGPitch];
+    __shared__ __align__(16) float Bs[2][kGK][kGPitch];
     __shared__ uint32_t s_rows[kGM];
     const int tid = threadIdx.x;
     const int tx = tid & 15;
@@ -397,50 +411,125 @@ __global__ void __launch_bounds__(256) matmul_id_grouped_simt_kernel(MatmulIdPar
     if (tid < kGM) s_rows[tid] = i0 + tid < cnt ? p.routed_rows[e * p.m + i0 + tid] : 0xffffffffu;
     __syncthreads();
     const TW *W = static_cast<const TW *>(p.w) + e * p.expert_stride_elems;
-    float acc[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
 
-    for (int64_t k0 = 0; k0 < p.k; k0 += kGK) {
+    // this thread's global sources
+    const int akc = (tid & 3) * 4;
+    const float *arow[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int idx = tid + q * 256;
-            const int x = idx % kGK;
-            const int i = idx / kGK;
-            const uint32_t rr = s_rows[i];
-            float v = 0.f;
-            if (rr != 0xffffffffu && k0 + x < p.k) v = x_row(p, rr)[k0 + x];
-            As[x][i] = v;
-            const int64_t gj = n0 + i;  // reuse the mapping for B rows (64 of them)
-            float w = 0.f;
-            if (gj < p.n && k0 + x < p.k) w = Elem<TW>::to_f(W[gj * p.k + k0 + x]);
-            Bs[x][i] = w;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int x = 0; x < kGK; ++x) {
-            float av[4], bv[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) av[r] = As[x][ty + 16 * r];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) bv[c] = Bs[x][tx + 16 * c];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
-        }
-        __syncthreads();
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t rr = s_rows[(tid >> 2) + 64 * h];
+        arow[h] = rr != 0xffffffffu ? x_row(p, rr) : nullptr;
     }
+    const int bcol0 = kV == 4 ? (tid >> 2) : (tid >> 1);
+    const int bkc = kV == 4 ? (tid & 3) * 4 : (tid & 1) * 8;
+
+    auto load = [&](int64_t k0, float4 (&ra)[2], float (&rb)[8]) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const uint32_t rr = s_rows[ty + 16 * r];
+        for (int h = 0; h < 2; ++h) {
+            const int64_t kx = k0 + akc;
+            if (arow[h] == nullptr) {
+                ra[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (vec_ok && kx + 4 <= p.k) {
+                ra[h] = *reinterpret_cast<const float4 *>(arow[h] + kx);
+            } else {
+                float v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = kx + j < p.k ? arow[h][kx + j] : 0.f;
+                ra[h] = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+        // weights: f32 -> 2 columns x 4 k; 16-bit -> 1 column x 8 k
+#pragma unroll
+        for (int h = 0; h < 8 / kV; ++h) {
+            const int64_t col = n0 + bcol0 + 64 * h;
+            const int64_t kx = k0 + bkc;
+            float *dst = rb + h * kV;
+            if (col >= p.n) {
+#pragma unroll
+                for (int j = 0; j < kV; ++j) dst[j] = 0.f;
+            } else if (vec_ok && kx + kV <= p.k) {
+                unpack16<TW>(ld_stream16(W + col * p.k + kx), dst);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kV; ++j) dst[j] = kx + j < p.k ? Elem<TW>::to_f(W[col * p.k + kx + j]) : 0.f;
+            }
+        }
+    };
+    auto store = [&](int buf, const float4 (&ra)[2], const float (&rb)[8]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = (tid >> 2) + 64 * h;
+            As[buf][akc + 0][r] = ra[h].x;
+            As[buf][akc + 1][r] = ra[h].y;
+            As[buf][akc + 2][r] = ra[h].z;
+            As[buf][akc + 3][r] = ra[h].w;
+        }
+#pragma unroll
+        for (int h = 0; h < 8 / kV; ++h) {
+            const int c = bcol0 + 64 * h;
+#pragma unroll
+            for (int j = 0; j < kV; ++j) Bs[buf][bkc + j][c] = rb[h * kV + j];
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+
+    // RN = 8: all 128 rows; RN = 4: the block holds at most 64 routed rows, so
+    // the upper 64 (all padding) are neither loaded nor multiplied
+    auto mainloop = [&](auto rows_c) {
+        constexpr int RN = decltype(rows_c)::value;
+        float4 ra[2];
+        float rb[8];
+        load(0, ra, rb);
+        store(0, ra, rb);
+        __syncthreads();
+        int cur = 0;
+        for (int64_t k0 = 0; k0 < p.k; k0 += kGK) {
+            const bool more = k0 + kGK < p.k;
+            if (more) load(k0 + kGK, ra, rb);
+#pragma unroll
+            for (int kk = 0; kk < kGK; ++kk) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][4 * ty]);
+                const float4 a1 = RN == 8 ? *reinterpret_cast<const float4 *>(&As[cur][kk][64 + 4 * ty]) : a0;
+                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][4 * tx]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][64 + 4 * tx]);
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int r = 0; r < RN; ++r)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+            }
+            if (more) store(cur ^ 1, ra, rb);
+            __syncthreads();
+            cur ^= 1;
+        }
+    };
+    if (cnt - i0 <= 64)
+        mainloop(std::integral_constant<int, 4>{});
+    else
+        mainloop(std::integral_constant<int, 8>{});
+
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const uint32_t rr = s_rows[(r < 4 ? 0 : 64) + 4 * ty + (r & 3)];
         if (rr == 0xffffffffu) continue;
+        float *orow = p.out + static_cast<int64_t>(rr) * p.n;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int64_t gj = n0 + tx + 16 * c;
-            if (gj < p.n) p.out[static_cast<int64_t>(rr) * p.n + gj] = acc[r][c];
+        for (int h = 0; h < 2; ++h) {
+            const int64_t c0 = n0 + 64 * h + 4 * tx;
+            if (out_vec_ok && c0 + 4 <= p.n) {
+                *reinterpret_cast<float4 *>(orow + c0) =
+                    make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2], acc[r][4 * h + 3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c0 + c < p.n) orow[c0 + c] = acc[r][4 * h + c];
+            }
         }
     }
 }
@@ -463,13 +552,13 @@ cudaError_t direct_t(const MatmulIdParams &p, int vec_ok, cudaStream_t s) {
 }
 
 template <typename TW>
-cudaError_t grouped_simt_t(const MatmulIdParams &p, cudaStream_t s) {
+cudaError_t grouped_simt_t(const MatmulIdParams &p, int vec_ok, int out_vec_ok, cudaStream_t s) {
     const int64_t gx = (p.m + kGM - 1) / kGM;
     const int64_t gy = (p.n + kGN - 1) / kGN;
     if (gx > 0x7fffffffLL || gy > 65535 || p.n_experts > 65535) return cudaErrorInvalidConfiguration;
     matmul_id_grouped_simt_kernel<TW><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                                              static_cast<unsigned>(p.n_experts)),
-                                        256, 0, s>>>(p);
+                                        kGThreads, 0, s>>>(p, vec_ok, out_vec_ok);
     return cudaGetLastError();
 }
 
@@ -526,10 +615,17 @@ cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s) {
+    // 16-byte vectors need 16-byte aligned expert rows and activation rows
+    const int size = dtype_size(wdt);
+    const int vec_ok = (reinterpret_cast<uintptr_t>(p.w) % 16 == 0) && ((p.expert_stride_elems * size) % 16 == 0) &&
+                       ((p.k * size) % 16 == 0) && ((p.k * 4) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(p.x) % 16 == 0) && ((p.x_token_stride * 4) % 16 == 0) &&
+                       ((p.x_slot_stride * 4) % 16 == 0);
+    const int out_vec_ok = (reinterpret_cast<uintptr_t>(p.out) % 16 == 0) && (p.n % 4 == 0);
     switch (wdt) {
-    case kF32: return grouped_simt_t<float>(p, s);
-    case kF16: return grouped_simt_t<__half>(p, s);
-    case kBF16: return grouped_simt_t<__nv_bfloat16>(p, s);
+    case kF32: return grouped_simt_t<float>(p, vec_ok, out_vec_ok, s);
+    case kF16: return grouped_simt_t<__half>(p, vec_ok, out_vec_ok, s);
+    case kBF16: return grouped_simt_t<__nv_bfloat16>(p, vec_ok, out_vec_ok, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -397,6 +397,26 @@ def test_skinny_tensor_core_exact_small_integers(oracle_mod, dtype):
     assert np.array_equal(got, rounded)
 
 
+SKINNY_SPLIT_CASES = [
+    # dtype, m, n, k, lda, ldc: what the case covers (cluster split chosen by the library)
+    ("f16", 5, 300, 1000, None, None),    # ragged k (15 blocks + 40), 3 tiles, a 3-way split of 16 k-blocks
+    ("bf16", 2, 129, 8, None, None),      # one partial k-block, no split, a one-row last tile
+    ("f16", 15, 128, 4096, None, 136),    # one tile, 8-way split, C rows padded (gaps must stay untouched)
+    ("bf16", 9, 2000, 520, 528, None),    # padded x rows, 9 k-blocks split 2 ways (4 and 5)
+    ("f16", 3, 11008, 64, None, None),    # one whole k-block per tile, 86 tiles
+]
+
+
+@pytest.mark.parametrize("case", SKINNY_SPLIT_CASES, ids=lambda c: f"{c[0]}_m{c[1]}_n{c[2]}_k{c[3]}")
+def test_skinny_tensor_core_splits_and_tails(oracle_mod, case):
+    """The skinny tensor-core GEMV across its k splits (1 to 8 CTAs per tile
+    adding partial sums through distributed shared memory) and its ragged
+    edges; every output against the oracle."""
+    dtype, m, n, k, lda, ldc = case
+    g = StridedGemm(dtype, 1, m, n, k, False, True, lda=lda, ldc=ldc, std=1.0 / np.sqrt(k), seed=n + k)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemv_tc")
+
+
 # ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------

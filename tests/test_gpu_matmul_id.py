@@ -351,6 +351,23 @@ def test_no_id_in_range(oracle_mod, route):
         assert np.all(r.counts.read(np.uint32, E) == 0)
 
 
+@pytest.mark.parametrize("wdtype", ["f32", "f16"])
+def test_grouped_ffma_row_block_sizes(oracle_mod, wdtype):
+    """The FFMA grouped kernel's row blocks of 128 routed rows, and its
+    half-block path for blocks of at most 64: expert lists of 64, 65, 1, 129
+    and 0 rows (top-1 routing, so each token's id is its expert), ragged n and
+    k; every output and the map."""
+    sizes = [64, 65, 1, 129, 0]
+    ids = np.concatenate([np.full(c, e, dtype=np.uint32) for e, c in enumerate(sizes)])
+    ids = np.random.default_rng(11).permutation(ids).reshape(-1, 1)
+    m, E = ids.shape[0], len(sizes)
+    case = synth.matmul_id_case("ffma_blocks", wdtype, m, 200, 52, 1, E, route=1, ids=ids)
+    r = Run(case).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_simt"
+    r.check(oracle_mod)
+    r.check_map(oracle_mod)
+
+
 def test_grouped_max_experts(oracle_mod):
     """n_experts = 1024, the grouped route's limit: 1200 routed rows over 1024
     experts (most lists hold 0 to 3 rows).  Every output and the map."""
