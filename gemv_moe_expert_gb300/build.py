@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgbmm.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["api.cu", "gemv.cu", "gemv_tc.cu", "gemm_simt.cu", "gemm_tc.cu", "grouped_tc.cu", "matmul_id.cu",
+SOURCES = ["api.cu", "direct_tc.cu", "gemv.cu", "gemv_tc.cu", "gemm_simt.cu", "gemm_tc.cu", "grouped_tc.cu", "matmul_id.cu",
            "misc.cu", "static_scratch.cu", "stream.cu"]
 HEADERS = ["device_common.cuh", "kernel_params.h"]
 

@@ -7,6 +7,7 @@
 // `dispatch_metal_mlx_gemm`: operand layouts), mlx-native 0.13.0,
 // src/ops/dense_matmul_id.rs (`dense_matmul_id_capability`,
 // `validate_dense_matmul_id_call`, `dense_matmul_id`, `DenseMatmulIdScratch`).
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -601,6 +602,40 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
 
     if (!grouped) {
         if (!resolve("gbmm_matmul_id_direct")) return GBMM_ERR_KERNEL_UNAVAILABLE;
+        // tensor cores for bf16 weights read by TMA (16-byte aligned base,
+        // expert stride and rows) with at most direct_tc_max_ids() routed rows
+        CUtensorMap map_w;
+        bool tc = weight_dtype == GBMM_BF16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
+                  p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 &&
+                  mp.total_rows <= direct_tc_max_ids() && p->n_experts <= static_cast<uint32_t>(direct_tc_max_experts()) &&
+                  direct_tc_block_k() == 64;
+        if (tc) {
+            PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+            cuuint64_t wdims[3] = {p->k, p->n, p->n_experts};
+            cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(p->k) * 2, p->expert_stride_bytes};
+            cuuint32_t wbox[3] = {static_cast<cuuint32_t>(direct_tc_block_k()),
+                                  static_cast<cuuint32_t>(direct_tc_block_rows()), 1u};
+            cuuint32_t estr[3] = {1u, 1u, 1u};
+            tc = enc != nullptr &&
+                 enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), wdims, wstrides, wbox,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+        if (tc) {
+            mp.err = device_error_word();
+            if (mp.err == nullptr) return fail(GBMM_ERR_CUDA, "%s: device error word unavailable", fn);
+            const int64_t max_distinct = std::min<int64_t>(p->n_experts, mp.total_rows);
+            // a cluster split of k needs one pass per expert: at most 16 routed
+            // rows can choose one expert whatever the ids are
+            const int split = direct_tc_split(p->n, p->k, max_distinct, mp.total_rows, device_sm_count());
+            const int x_vec_ok = aligned(input, 16) && (mp.x_token_stride % 4 == 0) && (mp.x_slot_stride % 4 == 0);
+            st = after_launch(launch_matmul_id_direct_tc(map_w, mp, static_cast<int>(max_distinct), split, x_vec_ok,
+                                                         stream),
+                              "gbmm_matmul_id_direct_tc", stream);
+            if (st != GBMM_OK) return st;
+            if (receipt) *receipt = gbmm_matmul_id_receipt{static_cast<uint32_t>(weight_dtype), p->route, 1};
+            return GBMM_OK;
+        }
         st = after_launch(launch_matmul_id_direct(weight_dtype, mp, stream), "gbmm_matmul_id_direct",
                           stream);
         if (st != GBMM_OK) return st;

@@ -102,7 +102,32 @@ def test_direct_decode_workload_c4(oracle_mod):
     """m=4, E=64, top_k=8 distinct uniform ids, k=2048, n=1408, bf16 W: every output."""
     r = Run(synth.workload("c4_moe_direct")).call()
     r.check(oracle_mod)
-    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_direct"
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_direct_tc"
+
+
+DIRECT_TC_CASES = [
+    # m, top_k, E, n, k, layout: what the case covers
+    (1, 2, 8, 1408, 2048, 0),    # 2 routed rows: k split over clusters of 8 CTAs
+    (2, 8, 64, 1408, 2048, 1),   # 16 rows, Slotted: 176 CTAs, no split
+    (1, 4, 4, 300, 1000, 0),     # ragged n and k (15 k-blocks + 40), clusters of 4
+    (40, 8, 16, 256, 512, 0),    # 320 rows over 16 experts: several 16-row passes per expert, no split
+    (9, 1, 1024, 136, 64, 1),    # one k-block, 9 of 1024 experts
+]
+
+
+@pytest.mark.parametrize("case", DIRECT_TC_CASES, ids=lambda c: "m{}_top{}_E{}_n{}_k{}_l{}".format(*c))
+def test_direct_tensor_core_splits_and_passes(oracle_mod, case):
+    """The Direct route's tensor-core kernel across its k splits, its 16-row
+    passes and ragged edges, with out-of-range ids mixed in; every output."""
+    m, top_k, E, n, k, layout = case
+    ids = synth.distinct_ids(m, top_k, E, seed=n + k, zipf_s=None)
+    ids[0, top_k - 1] = E          # an out-of-range id: the row must be zero
+    c = synth.matmul_id_case(f"dtc-{m}-{E}", "bf16", m, n, k, top_k, E, route=0, input_layout=layout,
+                             ids=ids, seed=n + k)
+    r = Run(c).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_direct_tc"
+    r.check(oracle_mod)
+    assert np.all(r.output().reshape(m, top_k, n)[0, top_k - 1] == 0.0)
 
 
 @pytest.mark.parametrize("wdtype", synth.DTYPES)
