@@ -240,16 +240,19 @@ class Problem:
             return [self.a, self.b]
         return [self.wt, self.x, self.ids]
 
-    def call(self, stream):
+    def call(self, stream, inputs=None):
+        """One call on `stream`; `inputs` (same order as device_inputs()) swaps
+        in another copy of the input buffers."""
         gb, w = self.gb, self.w
+        ins = inputs if inputs is not None else self.device_inputs()
         if self.key in ("c1", "c2", "c3"):
             fn = gb.gbmm_gemv if self.key == "c2" else gb.gbmm_gemm
-            st = fn(w.dtype, w.batch, w.m, w.n, w.k, w.ta, w.tb, self.a, 0, w.lda, w.stride_a,
-                    self.b, 0, w.ldb, w.stride_b, self.c, 0, w.ldc, w.stride_c, stream)
+            st = fn(w.dtype, w.batch, w.m, w.n, w.k, w.ta, w.tb, ins[0], 0, w.lda, w.stride_a,
+                    ins[1], 0, w.ldb, w.stride_b, self.c, 0, w.ldc, w.stride_c, stream)
         else:
             c = w
-            st, _ = gb.gbmm_matmul_id(self.params, c.wdtype, self.wt, c.w.nbytes, self.x,
-                                      c.x.nbytes, self.ids, c.ids.nbytes, self.out,
+            st, _ = gb.gbmm_matmul_id(self.params, c.wdtype, ins[0], c.w.nbytes, ins[1],
+                                      c.x.nbytes, ins[2], c.ids.nbytes, self.out,
                                       self.cap.required_output_bytes, self.scratch, stream)
         if st != gb.GBMM_OK:
             raise RuntimeError(f"{self.key}: {gb.gbmm_status_string(st)}: {gb.gbmm_last_error()}")
@@ -473,6 +476,35 @@ def run_ours(args) -> None:
                           "bf16 rounding of the activations, half the tensor work; default splits "
                           "x = hi + lo); timed alone after an L2 flush"}
 
+    # side measurement (not part of the step): each call alone, launched back
+    # to back, its inputs rotated over enough device copies that every launch
+    # reads them from HBM (ceil(4 x L2 / working set) copies, none for the
+    # latency-bound small GEMM): the per-call time without an event between
+    # launches
+    steady = None
+    if not args.no_steady:
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        steady = {}
+        for k in keys:
+            p = probs[k]
+            ws = works[k]["bytes"]
+            copies = 1 if (k == "c1" or ws >= 4 * l2) else min(8, -(-4 * l2 // ws))
+            sets = [p.device_inputs()] + [[t.clone() for t in p.device_inputs()] for _ in range(copies - 1)]
+            n_iter = 50
+            for i in range(3):
+                p.call(sptr, sets[i % copies])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(n_iter):
+                p.call(sptr, sets[i % copies])
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n_iter
+            steady[k] = {"ms": ms, "frac_of_roofline": roof[k] * 1e3 / ms, "input_copies": int(copies)}
+            del sets
+        torch.cuda.empty_cache()
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -528,6 +560,10 @@ def run_ours(args) -> None:
                                     "between every two launches (those events are kept out of the timed "
                                     "steps)"),
                    "calls_split_ms": per_call_split,
+                   "calls_steady": steady,
+                   "calls_steady_timing": ("each call alone, 50 launches back to back between two events, "
+                                           "inputs rotated over input_copies device copies so that every "
+                                           "launch reads them from HBM (not part of the step)"),
                    "c5_single_rounding_option": single},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk, "wall_s_timed": wall,
@@ -786,6 +822,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-scale", type=float, default=1.0)
     ap.add_argument("--no-options", action="store_true", help="skip the opt-in mode side timings")
+    ap.add_argument("--no-steady", action="store_true", help="skip the per-call back-to-back timings")
     ap.add_argument("--sweep", choices=["crossover", "skinny", "dtypes"], default=None,
                     help="instead of the step: crossover = Direct against GroupedPrefill for m = 1..512; "
                          "skinny = the decode GEMV for m = 1..15; dtypes = the expert-ID matmul for every "
