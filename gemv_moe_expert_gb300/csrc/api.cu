@@ -602,10 +602,10 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
 
     if (!grouped) {
         if (!resolve("gbmm_matmul_id_direct")) return GBMM_ERR_KERNEL_UNAVAILABLE;
-        // tensor cores for bf16 weights read by TMA (16-byte aligned base,
+        // tensor cores for bf16 / f16 weights read by TMA (16-byte aligned base,
         // expert stride and rows) with at most direct_tc_max_ids() routed rows
         CUtensorMap map_w;
-        bool tc = weight_dtype == GBMM_BF16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
+        bool tc = (weight_dtype == GBMM_BF16 || weight_dtype == GBMM_F16) && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
                   p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 &&
                   mp.total_rows <= direct_tc_max_ids() && p->n_experts <= static_cast<uint32_t>(direct_tc_max_experts()) &&
                   direct_tc_block_k() == 64;
@@ -617,8 +617,10 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
                                   static_cast<cuuint32_t>(direct_tc_block_rows()), 1u};
             cuuint32_t estr[3] = {1u, 1u, 1u};
             tc = enc != nullptr &&
-                 enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), wdims, wstrides, wbox,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 enc(&map_w,
+                     weight_dtype == GBMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(weights), wdims, wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
         if (tc) {
@@ -629,8 +631,8 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
             // rows can choose one expert whatever the ids are
             const int split = direct_tc_split(p->n, p->k, max_distinct, mp.total_rows, device_sm_count());
             const int x_vec_ok = aligned(input, 16) && (mp.x_token_stride % 4 == 0) && (mp.x_slot_stride % 4 == 0);
-            st = after_launch(launch_matmul_id_direct_tc(map_w, mp, static_cast<int>(max_distinct), split, x_vec_ok,
-                                                         stream),
+            st = after_launch(launch_matmul_id_direct_tc(weight_dtype, map_w, mp, static_cast<int>(max_distinct), split,
+                                                         x_vec_ok, stream),
                               "gbmm_matmul_id_direct_tc", stream);
             if (st != GBMM_OK) return st;
             if (receipt) *receipt = gbmm_matmul_id_receipt{static_cast<uint32_t>(weight_dtype), p->route, 1};

@@ -1,5 +1,5 @@
 // direct_tc.cu -- the Direct route of the expert-ID matmul on the sm_103a
-// tensor cores, for bf16 expert weights and f32 activations.
+// tensor cores, for bf16 or f16 expert weights and f32 activations.
 //
 // Semantics: mlx-native 0.13.0, src/ops/dense_matmul_id.rs,
 // `dense_matmul_id` (Direct: for routed row r = t*top_k + s with
@@ -15,7 +15,14 @@
 // (hi = bf16(x), lo = bf16(x - hi), relative error <= 2^-16) and the two
 // halves are the two 16-row halves of one N = 32 operand, so each K = 16
 // step is a single MMA and the epilogue adds accumulator columns c and
-// c + 16.
+// c + 16.  f16 weights need f16 activations (one MMA takes one operand
+// type), and f16's 5-bit exponent cannot hold every f32: each routed row is
+// first scaled by a power of two that puts its largest magnitude over this
+// CTA's k-range in [2^14, 2^15) (one warp per row reads the row once before
+// its first k-block), split into f16 hi + lo (relative error <= 2^-22 for
+// elements within 2^-10 of that maximum, absolute <= 2^-25 in scaled units
+// below), and its accumulator column is scaled back exactly before any
+// partial sums are added.
 //
 // Grid: one CTA per (distinct-expert index d, 128-row weight tile, k-split
 // rank).  The host sizes it for min(n_experts, m * top_k) distinct experts,
@@ -64,14 +71,15 @@ constexpr int kMaxIds = 1024;
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxSplit = 8;
 constexpr uint32_t kTmemCols = 32;
-constexpr int kNumBars = 2 * kStages + 3;
+constexpr int kNumBars = 2 * kStages + 5;  // full, empty, tfull, tempty, drain, scale-ready x 2
 constexpr uint32_t kRingBytes = kStages * kStageBytes;
 constexpr uint32_t kIdsOff = kRingBytes;
 constexpr uint32_t kRowsOff = kIdsOff + kMaxIds * 4;
 constexpr uint32_t kMapOff = kRowsOff + kMaxIds * 4;
 constexpr uint32_t kBarOff = kMapOff + kMaxExperts / 8;
 constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kCtlOff + 32 + 1024;
+constexpr uint32_t kScaleOff = kCtlOff + 32;  // [2][kBR] f32 row scales + [2][kBR] inverses (f16 weights)
+constexpr uint32_t kSmemBytes = kScaleOff + 4 * kBR * 4 + 1024;
 static_assert(kStageBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kBM * kBR * 4 <= kRingBytes, "the partial sums are parked in the ring");
 static_assert(3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
@@ -84,12 +92,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __device__ __forceinline__ float bf16_lo_half(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi_half(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t packed) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&packed));
+}
+
+// hi = round(a), lo = round(a - hi) for a pair, in the 16-bit type of the weights
+template <bool kF16>
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint32_t &lo) {
+    if (kF16) {
+        hi = pack_f16x2(a, b);
+        const float2 h = f16x2_to_float2(hi);
+        lo = pack_f16x2(a - h.x, b - h.y);
+    } else {
+        hi = pack_bf16x2(a, b);
+        lo = pack_bf16x2(a - bf16_lo_half(hi), b - bf16_hi_half(hi));
+    }
+}
+
 __device__ __forceinline__ const float *x_row_of(const MatmulIdParams &p, uint32_t r) {
     const int64_t t = r / p.top_k;
     const int64_t s = r % p.top_k;
     return p.x + t * p.x_token_stride + s * p.x_slot_stride;
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 3)
 direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams p, int ksplit, int tiles,
                  int x_vec_ok) {
@@ -107,6 +138,9 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
     const uint32_t tfull_bar = bar0 + 8u * (2 * kStages);
     const uint32_t tempty_bar = tfull_bar + 8u;
     const uint32_t drain_bar = tfull_bar + 16u;
+    auto sready_bar = [&](int b) { return tfull_bar + 24u + 8u * b; };  // row scales of a pass written
+    float *scale_s = reinterpret_cast<float *>(smem + kScaleOff);  // [2][kBR] row scales, by pass parity
+    float *unscale_s = scale_s + 2 * kBR;                             // [2][kBR] their inverses
     uint32_t *ctl = reinterpret_cast<uint32_t *>(smem + kCtlOff);  // tmem slot, abort, expert, count
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctl + 1);
 
@@ -130,6 +164,8 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
         mbar_init(tfull_bar, 1);
         mbar_init(tempty_bar, 4);
         mbar_init(drain_bar, 1);
+        mbar_init(sready_bar(0), 4);
+        mbar_init(sready_bar(1), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -228,7 +264,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t kIdesc = idesc_f16(1u, kBM, kBN);  // bf16 x bf16 -> f32
+            constexpr uint32_t kIdesc = idesc_f16(kF16 ? 0u : 1u, kBM, kBN);  // 16-bit x 16-bit -> f32
             bool ok = true;
             int it = 0;
             for (int pass = 0; pass < passes && ok; ++pass) {
@@ -275,8 +311,55 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
         for (int pass = 0; pass < passes; ++pass) {
             const int c = pass * kBR + row;
             const float *src = c < cnt ? x_row_of(p, rows_s[c]) : nullptr;
-            bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+            float scale = 1.f;  // power of two applied before the f16 split
+            bool sok = true;
+            if (kF16) {
+                // row scales: activation warp w takes rows w, w + 4, w + 8, w + 12 of the
+                // pass, its lanes reading the row's k-range with 16-byte loads
+                const int b = pass & 1;
+                for (int rr = warp - 2; rr < kBR; rr += 4) {
+                    const int cr = pass * kBR + rr;
+                    float mx = 0.f;
+                    if (cr < cnt) {
+                        const float *xs = x_row_of(p, rows_s[cr]);
+                        const int64_t k_lo = static_cast<int64_t>(kb0) * kBK;
+                        const int64_t k_hi = min(p.k, static_cast<int64_t>(kb0 + kblocks) * kBK);
+                        if (x_vec_ok) {
+                            const float4 *x4 = reinterpret_cast<const float4 *>(xs);
+#pragma unroll 8
+                            for (int64_t q = k_lo / 4 + lane; q < k_hi / 4; q += 32) {
+                                const float4 a = x4[q];
+                                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+                            }
+                        } else {
+                            for (int64_t q = k_lo + lane; q < k_hi; q += 32) mx = fmaxf(mx, fabsf(xs[q]));
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    }
+                    // mx in [2^(eb-127), 2^(eb-126)): scale by 2^(141 - eb), kept within the normal range
+                    int sexp = 0;
+                    if (mx > 0.f) {
+                        const int eb = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu);
+                        sexp = min(126, max(-126, 141 - eb));
+                    }
+                    if (lane == 0) {
+                        scale_s[b * kBR + rr] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
+                        unscale_s[b * kBR + rr] = __uint_as_float(static_cast<uint32_t>(127 - sexp) << 23);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready_bar(b));
+                // every activation warp's rows
+                int r_ok = 0;
+                if (lane == 0) r_ok = mbar_wait_bounded(sready_bar(b), static_cast<uint32_t>(pass >> 1) & 1u, lim, abort_flag);
+                r_ok = __shfl_sync(0xffffffffu, r_ok, 0);
+                __syncwarp();
+                sok = r_ok != 0;
+                if (sok) scale = scale_s[b * kBR + row];
+            }
+            bool ok = sok;
+            for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
                 const int stage = it % kStages;
                 const uint32_t use = static_cast<uint32_t>(it / kStages);
                 int ready = 1;
@@ -303,10 +386,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
                 }
                 uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    hi[h] = pack_bf16x2(f[2 * h], f[2 * h + 1]);
-                    lo[h] = pack_bf16x2(f[2 * h] - bf16_lo_half(hi[h]), f[2 * h + 1] - bf16_hi_half(hi[h]));
-                }
+                for (int h = 0; h < 4; ++h) split_pair<kF16>(f[2 * h] * scale, f[2 * h + 1] * scale, hi[h], lo[h]);
                 // 128-byte swizzle: 16-byte chunk ch of operand row i at chunk ch ^ (i % 8)
                 const uint32_t xb = s0 + stage * kStageBytes + kWBytes;
                 const uint32_t a_hi = xb + static_cast<uint32_t>(row) * 128u + ((ch ^ (row & 7)) << 4);
@@ -338,6 +418,20 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
             tmem_ld_wait();
 #pragma unroll
             for (int cc = 0; cc < kBR; ++cc) acc[cc] = __uint_as_float(v[cc]) + __uint_as_float(v[cc + kBR]);
+            if (kF16) {
+                // every activation warp has written its rows' scales for this pass
+                int sok = 0;
+                if (lane == 0)
+                    sok = mbar_wait_bounded(sready_bar(pass & 1), static_cast<uint32_t>(pass >> 1) & 1u, lim, abort_flag);
+                sok = __shfl_sync(0xffffffffu, sok, 0);
+                __syncwarp();
+                if (!sok && lane == 0) {
+                    *abort_flag = 1;
+                    report_device_error(p.err, kKidDirectTc);
+                }
+#pragma unroll
+                for (int cc = 0; cc < kBR; ++cc) acc[cc] *= unscale_s[(pass & 1) * kBR + cc];
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar);
@@ -415,17 +509,16 @@ int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows
     return split;
 }
 
-cudaError_t launch_matmul_id_direct_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int max_distinct,
-                                       int ksplit, int x_vec_ok, cudaStream_t s) {
-    if (ksplit < 1 || ksplit > kMaxSplit || max_distinct < 1 || p.total_rows > kMaxIds ||
-        p.n_experts > kMaxExperts)
-        return cudaErrorInvalidValue;
+namespace {
+template <bool kF16>
+cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int max_distinct, int ksplit,
+                        int x_vec_ok, cudaStream_t s) {
     static unsigned long long attr_set = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(direct_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(direct_tc_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
@@ -445,7 +538,20 @@ cudaError_t launch_matmul_id_direct_tc(const CUtensorMap &map_w, const MatmulIdP
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, direct_tc_kernel, map_w, p, ksplit, static_cast<int>(tiles), x_vec_ok);
+    return cudaLaunchKernelEx(&cfg, direct_tc_kernel<kF16>, map_w, p, ksplit, static_cast<int>(tiles), x_vec_ok);
+}
+}  // namespace
+
+cudaError_t launch_matmul_id_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
+                                       int max_distinct, int ksplit, int x_vec_ok, cudaStream_t s) {
+    if (ksplit < 1 || ksplit > kMaxSplit || max_distinct < 1 || p.total_rows > kMaxIds ||
+        p.n_experts > kMaxExperts)
+        return cudaErrorInvalidValue;
+    switch (wdt) {
+    case kF16: return direct_tc_t<true>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
+    case kBF16: return direct_tc_t<false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace gbmm

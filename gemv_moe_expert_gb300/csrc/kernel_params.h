@@ -138,12 +138,12 @@ cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulId
                                         int split, int num_sms, cudaStream_t s);
 cudaError_t launch_bounded_wait_test(uint32_t *err, uint64_t limit_ns, cudaStream_t s);
 int grouped_tc_max_experts();
-// Direct route on the tensor cores (direct_tc.cu): bf16 weights through a
-// 3-D tensor map over (k, n, expert) with direct_tc_block_k() x
-// direct_tc_block_rows() boxes; at most direct_tc_max_ids() routed rows and
+// Direct route on the tensor cores (direct_tc.cu): bf16 or f16 weights
+// (wdt) through a 3-D tensor map over (k, n, expert) with direct_tc_block_k()
+// x direct_tc_block_rows() boxes; at most direct_tc_max_ids() routed rows and
 // direct_tc_max_experts() experts
-cudaError_t launch_matmul_id_direct_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int max_distinct,
-                                       int ksplit, int x_vec_ok, cudaStream_t s);
+cudaError_t launch_matmul_id_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
+                                       int max_distinct, int ksplit, int x_vec_ok, cudaStream_t s);
 int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows_per_expert, int num_sms);
 int direct_tc_max_ids();
 int direct_tc_max_experts();

@@ -260,9 +260,10 @@ GBMM_API gbmm_status gbmm_matmul_id_capability(gbmm_dtype weight_dtype, const gb
  * Routes:
  *   Direct: one launch; each distinct expert selected by the call is
  *     streamed from HBM once and applied to every row that selected it (bf16
- *     weights with 16-byte aligned rows and at most 1024 routed rows: on the
- *     tensor cores, activations split exactly into bf16 hi + lo; otherwise
- *     on the FFMA pipe).
+ *     or f16 weights with 16-byte aligned rows and at most 1024 routed rows:
+ *     on the tensor cores, activations split into hi + lo of the weights'
+ *     type -- for f16 each routed row first scaled by a power of two into
+ *     f16's range, and scaled back exactly; otherwise on the FFMA pipe).
  *   GroupedPrefill: two launches in stream order -- the routing map
  *     (expert_counts / routed_rows, atomic-free count / scan / scatter; also
  *     zero-fills rows with out-of-range ids), then the grouped tensor-core

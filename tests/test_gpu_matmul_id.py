@@ -115,19 +115,39 @@ DIRECT_TC_CASES = [
 ]
 
 
+@pytest.mark.parametrize("wdtype", ["bf16", "f16"])
 @pytest.mark.parametrize("case", DIRECT_TC_CASES, ids=lambda c: "m{}_top{}_E{}_n{}_k{}_l{}".format(*c))
-def test_direct_tensor_core_splits_and_passes(oracle_mod, case):
+def test_direct_tensor_core_splits_and_passes(oracle_mod, case, wdtype):
     """The Direct route's tensor-core kernel across its k splits, its 16-row
     passes and ragged edges, with out-of-range ids mixed in; every output."""
     m, top_k, E, n, k, layout = case
     ids = synth.distinct_ids(m, top_k, E, seed=n + k, zipf_s=None)
     ids[0, top_k - 1] = E          # an out-of-range id: the row must be zero
-    c = synth.matmul_id_case(f"dtc-{m}-{E}", "bf16", m, n, k, top_k, E, route=0, input_layout=layout,
+    c = synth.matmul_id_case(f"dtc-{m}-{E}", wdtype, m, n, k, top_k, E, route=0, input_layout=layout,
                              ids=ids, seed=n + k)
     r = Run(c).call()
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_direct_tc"
     r.check(oracle_mod)
     assert np.all(r.output().reshape(m, top_k, n)[0, top_k - 1] == 0.0)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_direct_tensor_core_f16_activation_range(oracle_mod, split):
+    """f16 weights take f16 activations on the tensor cores, each routed row
+    scaled by a power of two first: rows of magnitude 1e30, 1e-30 and 7e4
+    (above f16's largest finite value), a zero row and a row whose elements
+    span 2^24 still meet 2e-3 * sum|w||x|.  With two routed rows the k-blocks
+    are split over a cluster (each CTA scales over its own k-range)."""
+    m, top_k, E, n, k = (1, 2, 8, 1408, 2048) if split else (6, 2, 8, 264, 512)
+    c = synth.matmul_id_case("f16range", "f16", m, n, k, top_k, E, route=0, input_layout=1, seed=21)
+    rows = c.x.reshape(m * top_k, k)
+    factors = [1e30, 1e-30, 7e4, 0.0, 1.0, 3.0e-3][: m * top_k]
+    for r, f in enumerate(factors):
+        rows[r] *= np.float32(f)
+    rows[-1] *= np.exp2(np.linspace(-12, 12, k)).astype(np.float32)
+    r = Run(c).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_direct_tc"
+    r.check(oracle_mod)
 
 
 @pytest.mark.parametrize("wdtype", synth.DTYPES)
