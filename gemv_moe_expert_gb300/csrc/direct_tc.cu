@@ -499,13 +499,16 @@ int direct_tc_block_k() { return kBK; }
 
 int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows_per_expert, int num_sms) {
     // a cluster split only when one pass covers every expert's rows; the
-    // largest that keeps the grid within 1.25 CTAs per SM with at least four
-    // k-blocks per CTA (the rule of the skinny GEMV)
+    // largest that keeps the grid within one wave of three CTAs per SM with
+    // at least four k-blocks per CTA.  A CTA keeps only three 16 KB weight
+    // stages in flight (~30 GB/s alone), so a call with few experts needs
+    // the split to fill the SMs: 8 experts x 12 tiles (one token, top-8)
+    // took 45.7 us unsplit against 35.5 us on the FFMA kernel
     if (max_rows_per_expert > kBR) return 1;
     const int64_t units = (n + kBM - 1) / kBM * max_distinct;
     const int64_t kb = (k + kBK - 1) / kBK;
     int split = 1;
-    while (split < kMaxSplit && 4 * units * (split + 1) <= 5LL * num_sms && kb >= 4LL * (split + 1)) ++split;
+    while (split < kMaxSplit && units * (split + 1) <= 3LL * num_sms && kb >= 4LL * (split + 1)) ++split;
     return split;
 }
 

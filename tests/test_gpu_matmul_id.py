@@ -108,7 +108,7 @@ def test_direct_decode_workload_c4(oracle_mod):
 DIRECT_TC_CASES = [
     # m, top_k, E, n, k, layout: what the case covers
     (1, 2, 8, 1408, 2048, 0),    # 2 routed rows: k split over clusters of 8 CTAs
-    (2, 8, 64, 1408, 2048, 1),   # 16 rows, Slotted: 176 CTAs, no split
+    (2, 8, 64, 1408, 2048, 1),   # 16 rows, Slotted: 176 units, clusters of 2
     (1, 4, 4, 300, 1000, 0),     # ragged n and k (15 k-blocks + 40), clusters of 4
     (40, 8, 16, 256, 512, 0),    # 320 rows over 16 experts: several 16-row passes per expert, no split
     (9, 1, 1024, 136, 64, 1),    # one k-block, 9 of 1024 experts
