@@ -717,6 +717,43 @@ def _time_alone(call, torch, flush, steps, warmup):
     return statistics.median(ts)
 
 
+def run_ffma(args) -> None:
+    """The f32 GEMM on the FFMA pipe at compute-bound sizes (f32 has no
+    tensor-core route here): 4096^3 for every transpose pair and 2048^3 nt,
+    each call timed alone after an L2 flush, with its fraction of the FFMA
+    peak (152 SMs x 128 lanes x 2 flops at the sampled SM clock)."""
+    import torch
+    from gemv_moe_expert_gb300 import binding as gb
+    from gemv_moe_expert_gb300 import build
+    build.build()
+    gb.load()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rows = []
+    for (m, n, k, ta, tb) in [(4096, 4096, 4096, 0, 0), (4096, 4096, 4096, 0, 1), (4096, 4096, 4096, 1, 0),
+                              (4096, 4096, 4096, 1, 1), (2048, 2048, 2048, 0, 1)]:
+        a = torch.randn(m * k, device="cuda", generator=g) / np.sqrt(k)
+        b = torch.randn(n * k, device="cuda", generator=g)
+        c = torch.empty(m * n, device="cuda")
+        lda, ldb = (m if ta else k), (k if tb else n)
+
+        def call():
+            gb.check(gb.gbmm_gemm("f32", 1, m, n, k, ta, tb, a, 0, lda, m * k, b, 0, ldb, n * k, c, 0, n, m * n))
+
+        clocks = ClockSampler(0)
+        clocks.start()
+        us = _time_alone(call, torch, flush, args.steps, args.warmup)
+        clk = clocks.stop() or {}
+        peak = ffma_peak_tflops(clk.get("sm_mhz") or 2070.0)
+        tflops = 2 * m * n * k / (us * 1e-6) / 1e12
+        rows.append({"m": m, "n": n, "k": k, "ta": ta, "tb": tb, "us": us, "tflops": tflops,
+                     "ffma_peak_tflops": peak, "frac_of_ffma_peak": tflops / peak,
+                     "kernel": gb.gbmm_test_last_kernel(), "sm_mhz": clk.get("sm_mhz")})
+        del a, b, c
+    print(json.dumps({"sweep": "f32 GEMM on the FFMA pipe", "timing": "each call alone after an L2 flush, "
+                      "median of --steps", "rows": rows}), flush=True)
+
+
 def run_skinny(args) -> None:
     """The decode GEMV y[m, n] = x[m, k] W[n, k]^T (B stored [n, k], batch 1)
     for m = 1 .. 15 tokens on the decode workload's shape (n 11008, k 4096), f16
@@ -823,10 +860,10 @@ def main():
     ap.add_argument("--cpu-scale", type=float, default=1.0)
     ap.add_argument("--no-options", action="store_true", help="skip the opt-in mode side timings")
     ap.add_argument("--no-steady", action="store_true", help="skip the per-call back-to-back timings")
-    ap.add_argument("--sweep", choices=["crossover", "skinny", "dtypes"], default=None,
+    ap.add_argument("--sweep", choices=["crossover", "skinny", "dtypes", "ffma"], default=None,
                     help="instead of the step: crossover = Direct against GroupedPrefill for m = 1..512; "
                          "skinny = the decode GEMV for m = 1..15; dtypes = the expert-ID matmul for every "
-                         "weight dtype, input layout and id multiplicity")
+                         "weight dtype, input layout and id multiplicity; ffma = the f32 GEMM at 4096^3")
     args = ap.parse_args()
     args.only = [k.strip() for k in args.only.split(",") if k.strip()]
     if args.warmup < 3 and args.impl == "ours":
@@ -837,6 +874,8 @@ def main():
         run_skinny(args)
     elif args.sweep == "dtypes":
         run_dtypes(args)
+    elif args.sweep == "ffma":
+        run_ffma(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -7,9 +7,15 @@
 // [n, k] when transposed), and rlx-metal 0.2.14, src/mps_blas.rs,
 // `encode_mps_sgemm_t`.
 //
-// CTA tile 64 x 64 x 16, 256 threads, 4 x 4 outputs per thread; operands are
-// staged through shared memory as f32 with the global loads ordered along the
-// contiguous dimension of each operand (coalesced for every transpose flag).
+// Two tilings, both with operands staged through shared memory as f32 and the
+// global loads ordered along the contiguous dimension of each operand
+// (coalesced for every transpose flag):
+//   128 x 128 x 16 per CTA, 256 threads, 8 x 8 outputs per thread (four
+//   16-byte shared-memory reads per 64 FMAs), the next k step's tiles loaded
+//   into registers while the current one is multiplied (two buffers, one
+//   barrier per step) -- for grids of at least one 128 x 128 tile per SM;
+//   64 x 64 x 16, 4 x 4 outputs per thread -- for smaller grids, where the
+//   larger tile would leave SMs idle.
 #include "device_common.cuh"
 
 namespace gbmm {
@@ -100,6 +106,103 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmParams p) {
     }
 }
 
+constexpr int kWM = 128;
+constexpr int kWN = 128;
+constexpr int kWK = 16;
+constexpr int kWPitch = kWM + 4;  // keeps each k row of a tile 16-byte aligned
+
+template <typename T>
+__global__ void __launch_bounds__(256, 2) gemm_ffma128_kernel(GemmParams p, int c_vec_ok) {
+    __shared__ __align__(16) float As[2][kWK][kWPitch];
+    __shared__ __align__(16) float Bs[2][kWK][kWPitch];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kWM;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kWN;
+
+    for (int64_t bat = blockIdx.z; bat < p.batch; bat += gridDim.z) {
+        const T *A = static_cast<const T *>(p.a) + bat * p.sa;
+        const T *B = static_cast<const T *>(p.b) + bat * p.sb;
+        T *C = static_cast<T *>(p.c) + bat * p.sc;
+
+        // element e (< 8) of this thread's share of the 128 x 16 tiles: A as
+        // (row i, k x), B as (column j, k y), walked along the stored dimension
+        auto load = [&](int64_t k0, float (&ra)[8], float (&rb)[8]) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int idx = tid + 256 * e;  // 0 .. 2047
+                int i, x;
+                if (p.ta) { i = idx % kWM; x = idx / kWM; } else { x = idx % kWK; i = idx / kWK; }
+                const int64_t gi = m0 + i, gx = k0 + x;
+                ra[e] = (gi < p.m && gx < p.k) ? Elem<T>::to_f(A[p.ta ? gx * p.lda + gi : gi * p.lda + gx]) : 0.f;
+                int j, y;
+                if (p.tb) { y = idx % kWK; j = idx / kWK; } else { j = idx % kWN; y = idx / kWN; }
+                const int64_t gj = n0 + j, gy = k0 + y;
+                rb[e] = (gj < p.n && gy < p.k) ? Elem<T>::to_f(B[p.tb ? gj * p.ldb + gy : gy * p.ldb + gj]) : 0.f;
+            }
+        };
+        auto store = [&](int buf, const float (&ra)[8], const float (&rb)[8]) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int idx = tid + 256 * e;
+                if (p.ta) As[buf][idx / kWM][idx % kWM] = ra[e]; else As[buf][idx % kWK][idx / kWK] = ra[e];
+                if (p.tb) Bs[buf][idx % kWK][idx / kWK] = rb[e]; else Bs[buf][idx / kWN][idx % kWN] = rb[e];
+            }
+        };
+
+        float acc[8][8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+
+        float ra[8], rb[8];
+        load(0, ra, rb);
+        store(0, ra, rb);
+        __syncthreads();
+        int cur = 0;
+        for (int64_t k0 = 0; k0 < p.k; k0 += kWK) {
+            const bool more = k0 + kWK < p.k;
+            if (more) load(k0 + kWK, ra, rb);
+#pragma unroll
+            for (int kk = 0; kk < kWK; ++kk) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][4 * ty]);
+                const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][64 + 4 * ty]);
+                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][4 * tx]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][64 + 4 * tx]);
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+            }
+            if (more) store(cur ^ 1, ra, rb);
+            __syncthreads();
+            cur ^= 1;
+        }
+
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int64_t gi = m0 + (r < 4 ? 0 : 64) + 4 * ty + (r & 3);
+            if (gi >= p.m) continue;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t gj = n0 + 64 * h + 4 * tx;
+                if (c_vec_ok && gj + 4 <= p.n) {
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(C) + gi * p.ldc + gj) =
+                        make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2], acc[r][4 * h + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (gj + c < p.n) C[gi * p.ldc + gj + c] = Elem<T>::from_f(acc[r][4 * h + c]);
+                }
+            }
+        }
+    }
+}
+
 // Small problems are latency-bound.  A CTA owns 16 x 16 outputs; per chunk of
 // 128 along k it first issues every load of its A rows and B columns at once
 // (one memory round trip), stages them in shared memory as f32, then each
@@ -170,6 +273,21 @@ cudaError_t small_t(const GemmParams &p, cudaStream_t s) {
 
 template <typename T>
 cudaError_t simt_t(const GemmParams &p, cudaStream_t s) {
+    // the 128 x 128 tile once it gives every SM at least one CTA
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t wx = (p.n + kWN - 1) / kWN, wy = (p.m + kWM - 1) / kWM;
+    const int64_t wbatch = p.batch < 65535 ? p.batch : 65535;
+    if (wx * wy * wbatch >= sms && wx <= 0x7fffffffLL && wy <= 65535) {
+        // 16-byte f32 stores: C 16-byte aligned with rows and batches a multiple of 4 elements apart
+        const int c_vec_ok = sizeof(T) == 4 && reinterpret_cast<uintptr_t>(p.c) % 16 == 0 && p.ldc % 4 == 0 &&
+                             p.sc % 4 == 0;
+        gemm_ffma128_kernel<T><<<dim3(static_cast<unsigned>(wx), static_cast<unsigned>(wy),
+                                      static_cast<unsigned>(wbatch)),
+                                 256, 0, s>>>(p, c_vec_ok);
+        return cudaGetLastError();
+    }
     const int64_t gx = (p.n + kBN - 1) / kBN;
     const int64_t gy = (p.m + kBM - 1) / kBM;
     if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;

@@ -397,6 +397,26 @@ def test_skinny_tensor_core_exact_small_integers(oracle_mod, dtype):
     assert np.array_equal(got, rounded)
 
 
+FFMA_WIDE_CASES = [
+    # dtype, batch, m, n, k, ta, tb, lda, ldc: grids of >= 152 tiles of 128 x 128 take the wide FFMA tile
+    ("f32", 4, 1030, 650, 200, False, False, None, None),   # ragged m and n tails, nn
+    ("f32", 4, 1030, 650, 200, False, True, None, 656),     # nt, C rows padded (16-byte stores)
+    ("f32", 4, 1030, 650, 200, True, False, None, 651),     # tn, C rows padded to an odd pitch (scalar stores)
+    ("f32", 4, 1030, 650, 200, True, True, None, None),     # tt
+    ("f16", 2, 1664, 1536, 72, False, True, 75, None),      # f16 rows TMA cannot read (odd lda)
+]
+
+
+@pytest.mark.parametrize("case", FFMA_WIDE_CASES, ids=lambda c: "{}_b{}_{}x{}x{}_ta{}_tb{}".format(*c[:7]))
+def test_ffma_wide_tile_parity(oracle_mod, case):
+    """The 128 x 128 FFMA tile (8 x 8 outputs per thread, double-buffered
+    shared memory) for every transpose pair, ragged tails and padded rows;
+    every output against the oracle."""
+    dtype, batch, m, n, k, ta, tb, lda, ldc = case
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, lda=lda, ldc=ldc, std=1.0 / np.sqrt(k), seed=m + n + k)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+
+
 SKINNY_SPLIT_CASES = [
     # dtype, m, n, k, lda, ldc: what the case covers (cluster split chosen by the library)
     ("f16", 5, 300, 1000, None, None),    # ragged k (15 blocks + 40), 3 tiles, a 3-way split of 16 k-blocks
