@@ -45,6 +45,11 @@
 //               k-block, split into bf16 hi / lo, write the swizzled K-major
 //               operand; after it: tcgen05.ld, hi + lo, f32 stores (a warp
 //               writes 32 consecutive outputs of a routed row)
+// The same kernel serves the GroupedPrefill route for f16 weights (the
+// grouped tcgen05 kernel takes bf16 only): there the map launch has already
+// written each expert's routed rows, so CTA (e, tile) reads expert e's count
+// and row list from the scratch instead of selecting from the ids, and the
+// map launch has written the zero rows.
 // Every mbarrier wait is bounded; a timeout is recorded in the device error
 // word, the CTA waits (bounded) for its own copies and MMAs, still takes part
 // in the cluster barriers, releases its TMEM and returns.
@@ -120,7 +125,7 @@ __device__ __forceinline__ const float *x_row_of(const MatmulIdParams &p, uint32
     return p.x + t * p.x_token_stride + s * p.x_slot_stride;
 }
 
-template <bool kF16>
+template <bool kF16, bool kFromMap>
 __global__ void __launch_bounds__(kThreads, 3)
 direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams p, int ksplit, int tiles,
                  int x_vec_ok) {
@@ -174,6 +179,15 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
         tmem_alloc(smem_addr(ctl), kTmemCols);
         tmem_relinquish();
     }
+    if (kFromMap) {
+        // GroupedPrefill: the map launch wrote expert d's routed rows
+        if (threadIdx.x == 0) {
+            const uint32_t c0 = p.counts[d];
+            const uint32_t cm = c0 < static_cast<uint32_t>(p.m) ? c0 : static_cast<uint32_t>(p.m);
+            ctl[2] = cm > 0 ? static_cast<uint32_t>(d) : 0xffffffffu;
+            ctl[3] = cm;
+        }
+    } else {
     // ---- this CTA's expert: the d-th distinct in-range id, ascending ----
     for (int i = threadIdx.x; i < nwords; i += kThreads) emap[i] = 0u;
     __syncthreads();
@@ -224,12 +238,17 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
             ctl[3] = static_cast<uint32_t>(cnt);
         }
     }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl[0];
     const int e_sel = static_cast<int>(ctl[2]);
     const int cnt = static_cast<int>(ctl[3]);
+    // routed row c of this CTA's expert
+    auto row_of = [&](int c) -> uint32_t {
+        return kFromMap ? p.routed_rows[static_cast<int64_t>(e_sel) * p.m + c] : rows_s[c];
+    };
     const int passes = e_sel >= 0 ? (cnt + kBR - 1) / kBR : 0;
     const int kb_total = static_cast<int>((p.k + kBK - 1) / kBK);
     const int kb0 = static_cast<int>(static_cast<int64_t>(kb_total) * rank / ksplit);
@@ -310,7 +329,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
         int it = 0;
         for (int pass = 0; pass < passes; ++pass) {
             const int c = pass * kBR + row;
-            const float *src = c < cnt ? x_row_of(p, rows_s[c]) : nullptr;
+            const float *src = c < cnt ? x_row_of(p, row_of(c)) : nullptr;
             float scale = 1.f;  // power of two applied before the f16 split
             bool sok = true;
             if (kF16) {
@@ -321,7 +340,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
                     const int cr = pass * kBR + rr;
                     float mx = 0.f;
                     if (cr < cnt) {
-                        const float *xs = x_row_of(p, rows_s[cr]);
+                        const float *xs = x_row_of(p, row_of(cr));
                         const int64_t k_lo = static_cast<int64_t>(kb0) * kBK;
                         const int64_t k_hi = min(p.k, static_cast<int64_t>(kb0 + kblocks) * kBK);
                         if (x_vec_ok) {
@@ -437,7 +456,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
             if (lane == 0) mbar_arrive(tempty_bar);
             if (ksplit == 1 && j < p.n) {
                 for (int cc = 0; cc < kBR && pass * kBR + cc < cnt; ++cc)
-                    p.out[static_cast<int64_t>(rows_s[pass * kBR + cc]) * p.n + j] = acc[cc];
+                    p.out[static_cast<int64_t>(row_of(pass * kBR + cc)) * p.n + j] = acc[cc];
             }
         }
     }
@@ -469,13 +488,13 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
             }
             const int64_t j = static_cast<int64_t>(n0) + rrow;
             if (j < p.n)
-                for (int c = 0; c < kBR && c < cnt; ++c) p.out[static_cast<int64_t>(rows_s[c]) * p.n + j] = acc[c];
+                for (int c = 0; c < kBR && c < cnt; ++c) p.out[static_cast<int64_t>(row_of(c)) * p.n + j] = acc[c];
         }
         cluster.sync();  // keep every rank's shared memory alive until rank 0 has read it
     }
 
     // zero rows of out-of-range ids, once per output column
-    if (d == 0 && rank == 0 && warp >= 2) {
+    if (!kFromMap && d == 0 && rank == 0 && warp >= 2) {
         const int64_t j = static_cast<int64_t>(n0) + (warp & 3) * 32 + lane;
         if (j < p.n)
             for (int r = 0; r < n_ids; ++r)
@@ -513,7 +532,7 @@ int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows
 }
 
 namespace {
-template <bool kF16>
+template <bool kF16, bool kFromMap>
 cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int max_distinct, int ksplit,
                         int x_vec_ok, cudaStream_t s) {
     static unsigned long long attr_set = 0;  // one bit per device
@@ -521,7 +540,7 @@ cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int m
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(direct_tc_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(direct_tc_kernel<kF16, kFromMap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
@@ -541,7 +560,8 @@ cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int m
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, direct_tc_kernel<kF16>, map_w, p, ksplit, static_cast<int>(tiles), x_vec_ok);
+    return cudaLaunchKernelEx(&cfg, direct_tc_kernel<kF16, kFromMap>, map_w, p, ksplit, static_cast<int>(tiles),
+                              x_vec_ok);
 }
 }  // namespace
 
@@ -551,8 +571,18 @@ cudaError_t launch_matmul_id_direct_tc(int wdt, const CUtensorMap &map_w, const 
         p.n_experts > kMaxExperts)
         return cudaErrorInvalidValue;
     switch (wdt) {
-    case kF16: return direct_tc_t<true>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
-    case kBF16: return direct_tc_t<false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
+    case kF16: return direct_tc_t<true, false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
+    case kBF16: return direct_tc_t<false, false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_matmul_id_grouped_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
+                                               int x_vec_ok, cudaStream_t s) {
+    // one CTA per (expert, 128-row weight tile): the rows come from the map
+    if (p.n_experts < 1 || p.n_experts > 0x7fffffffLL) return cudaErrorInvalidValue;
+    switch (wdt) {
+    case kF16: return direct_tc_t<true, true>(map_w, p, static_cast<int>(p.n_experts), 1, x_vec_ok, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -145,6 +145,10 @@ int grouped_tc_max_experts();
 cudaError_t launch_matmul_id_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
                                        int max_distinct, int ksplit, int x_vec_ok, cudaStream_t s);
 int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows_per_expert, int num_sms);
+// GroupedPrefill with f16 weights on the same kernel: one CTA per (expert,
+// tile), the routed rows read from the map's scratch (counts, routed_rows)
+cudaError_t launch_matmul_id_grouped_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
+                                               int x_vec_ok, cudaStream_t s);
 int direct_tc_max_ids();
 int direct_tc_max_experts();
 int direct_tc_block_rows();

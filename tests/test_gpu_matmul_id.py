@@ -237,7 +237,8 @@ def test_matmul_id_parity_small(oracle_mod, wdtype, route, layout):
                                 route=route, input_layout=layout, stride_pad_elems=8, seed=3)
     Run(case).call().check(oracle_mod)
     if route == 1:
-        want = "gbmm_matmul_id_grouped_tc" if wdtype == "bf16" else "gbmm_matmul_id_grouped_simt"
+        want = {"bf16": "gbmm_matmul_id_grouped_tc", "f16": "gbmm_matmul_id_grouped_direct_tc",
+                "f32": "gbmm_matmul_id_grouped_simt"}[wdtype]
         assert gb.gbmm_test_last_kernel() == want
 
 
@@ -411,6 +412,22 @@ def test_grouped_ffma_row_block_sizes(oracle_mod, wdtype):
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_simt"
     r.check(oracle_mod)
     r.check_map(oracle_mod)
+
+
+def test_grouped_f16_tensor_core_passes_and_range(oracle_mod):
+    """GroupedPrefill with f16 weights on the tensor cores (the Direct kernel
+    reading the map's row lists): 1200 routed rows over 6 experts (up to ~13
+    passes of 16 rows per expert), ragged n and k, Slotted rows of magnitude
+    1e20, 1e-20 and 7e4 mixed in; every output and the map."""
+    m, top_k, E, n, k = 300, 4, 6, 264, 1000
+    c = synth.matmul_id_case("f16grouped", "f16", m, n, k, top_k, E, route=1, input_layout=1, seed=23)
+    rows = c.x.reshape(m * top_k, k)
+    rows[::7] *= np.float32(1e20)
+    rows[3::11] *= np.float32(1e-20)
+    rows[5::13] *= np.float32(7e4)
+    r = Run(c).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_direct_tc"
+    r.check(oracle_mod)
 
 
 def test_grouped_max_experts(oracle_mod):
