@@ -266,9 +266,12 @@ GBMM_API gbmm_status gbmm_matmul_id_capability(gbmm_dtype weight_dtype, const gb
  *     f16's range, and scaled back exactly; otherwise on the FFMA pipe).
  *   GroupedPrefill: two launches in stream order -- the routing map
  *     (expert_counts / routed_rows, atomic-free count / scan / scatter; also
- *     zero-fills rows with out-of-range ids), then the grouped tensor-core
- *     GEMM over each expert's row list.  The second launch reads the first's
- *     scratch; a later call may reuse the scratch on the same stream.
+ *     zero-fills rows with out-of-range ids), then the grouped GEMM over
+ *     each expert's row list (tensor cores for bf16 weights with hi + lo
+ *     activations, and for f16 weights with per-row scaled f16 hi + lo; FFMA
+ *     for f32 weights and strides TMA cannot read).  The second launch reads
+ *     the first's scratch; a later call may reuse the scratch on the same
+ *     stream.
  * Both kernels this call needs are resolved before the first launch; if one
  * is unavailable the call fails with nothing enqueued ([P2] `dense_matmul_id`
  * resolves every pipeline before touching the encoder).
