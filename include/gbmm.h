@@ -369,7 +369,12 @@ GBMM_API void gbmm_test_inject_kernel_failure(const char *name);
 GBMM_API uint64_t gbmm_test_launch_count(void);
 GBMM_API void gbmm_test_reset_launch_count(void);
 
-/* Name of the kernel of the most recent launch on this host thread. */
+/* Name of the kernel of the most recent launch on this host thread:
+ * "gbmm_gemm_tc", "gbmm_gemm_simt", "gbmm_gemm_small", "gbmm_gemv_stream",
+ * "gbmm_gemv_rowdot", "gbmm_gemv_coldot", "gbmm_gemv_tc", "gbmm_fill_zero",
+ * "gbmm_matmul_id_direct", "gbmm_matmul_id_direct_tc", "gbmm_matmul_id_map",
+ * "gbmm_matmul_id_grouped_tc", "gbmm_matmul_id_grouped_direct_tc",
+ * "gbmm_matmul_id_grouped_simt", and "gbmm_bounded_wait_test" for the wait test below. */
 GBMM_API const char *gbmm_test_last_kernel(void);
 
 /*
