@@ -785,7 +785,25 @@ def run_skinny(args) -> None:
             rows.append({"dtype": dt, "m": m, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
                          "frac_of_hbm": bytes_ / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6),
                          "kernel": gb.gbmm_test_last_kernel()})
-    print(json.dumps({"sweep": "skinny decode GEMV", "n": n, "k": k, "layout": "B stored [n, k], batch 1",
+    # the other GEMV orientations on the same 11008 x 4096 f16 matrix: the vector times B stored [k, n]
+    # (outputs contiguous in the matrix rows), and n == 1 with A stored [m, k] or [k, m]
+    w = (torch.randn(n * k, device="cuda", generator=g) * 0.02).half()
+    x = torch.randn(k, device="cuda", generator=g).half()
+    y = torch.empty(n, device="cuda", dtype=torch.float16)
+    for label, args_ in (("m1_B_stored_kn", (1, n, k, 0, 0, x, k, k, w, n, n * k, y, n, n)),
+                         ("n1_A_stored_mk", (n, 1, k, 0, 1, w, k, n * k, x, k, k, y, 1, n)),
+                         ("n1_A_stored_km", (n, 1, k, 1, 1, w, n, n * k, x, k, k, y, 1, n))):
+        mm, nn, kk, ta, tb, a_, lda, sa, b_, ldb, sb, c_, ldc, sc = args_
+
+        def call():
+            gb.check(gb.gbmm_gemv("f16", 1, mm, nn, kk, ta, tb, a_, 0, lda, sa, b_, 0, ldb, sb, c_, 0, ldc, sc))
+        us = _time_alone(call, torch, flush, args.steps, args.warmup)
+        bytes_ = (n * k + k + n) * 2
+        rows.append({"dtype": "f16", "orientation": label, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
+                     "frac_of_hbm": bytes_ / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6),
+                     "kernel": gb.gbmm_test_last_kernel()})
+    print(json.dumps({"sweep": "skinny decode GEMV", "n": n, "k": k, "layout": "B stored [n, k], batch 1 "
+                      "(plus the rows with an orientation)",
                       "timing": "each call alone after an L2 flush, median of --steps", "rows": rows}), flush=True)
 
 
