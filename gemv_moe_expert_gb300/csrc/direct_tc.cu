@@ -188,56 +188,56 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
             ctl[3] = cm;
         }
     } else {
-    // ---- this CTA's expert: the d-th distinct in-range id, ascending ----
-    for (int i = threadIdx.x; i < nwords; i += kThreads) emap[i] = 0u;
-    __syncthreads();
-    for (int r = threadIdx.x; r < n_ids; r += kThreads) {
-        const uint32_t e = p.ids[r];
-        ids_s[r] = e;
-        if (e < E) atomicOr(&emap[e >> 5], 1u << (e & 31));
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int sel = -1;
-        uint32_t base = 0;
-        for (int w0 = 0; w0 < nwords; w0 += 32) {
-            const uint32_t word = w0 + lane < nwords ? emap[w0 + lane] : 0u;
-            const uint32_t c = static_cast<uint32_t>(__popc(word));
-            uint32_t incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t excl = base + incl - c;
-            const uint32_t want = static_cast<uint32_t>(d);
-            int mine = -1;
-            if (sel < 0 && want >= excl && want < excl + c) {
-                uint32_t wbits = word;
-                for (uint32_t j = 0; j < want - excl; ++j) wbits &= wbits - 1u;  // drop the lower set bits
-                mine = (w0 + lane) * 32 + __ffs(static_cast<int>(wbits)) - 1;
-            }
-            const unsigned who = __ballot_sync(0xffffffffu, mine >= 0);
-            if (who != 0u) sel = __shfl_sync(0xffffffffu, mine, __ffs(static_cast<int>(who)) - 1);
-            base += __shfl_sync(0xffffffffu, incl, 31);
+        // ---- this CTA's expert: the d-th distinct in-range id, ascending ----
+        for (int i = threadIdx.x; i < nwords; i += kThreads) emap[i] = 0u;
+        __syncthreads();
+        for (int r = threadIdx.x; r < n_ids; r += kThreads) {
+            const uint32_t e = p.ids[r];
+            ids_s[r] = e;
+            if (e < E) atomicOr(&emap[e >> 5], 1u << (e & 31));
         }
-        // the routed rows that chose it, ascending
-        int cnt = 0;
-        if (sel >= 0) {
-            const unsigned lt = (1u << lane) - 1u;
-            for (int b = 0; b < n_ids; b += 32) {
-                const int r = b + lane;
-                const bool hit = r < n_ids && ids_s[r] == static_cast<uint32_t>(sel);
-                const unsigned bal = __ballot_sync(0xffffffffu, hit);
-                if (hit) rows_s[cnt + __popc(bal & lt)] = static_cast<uint32_t>(r);
-                cnt += __popc(bal);
+        __syncthreads();
+        if (warp == 0) {
+            int sel = -1;
+            uint32_t base = 0;
+            for (int w0 = 0; w0 < nwords; w0 += 32) {
+                const uint32_t word = w0 + lane < nwords ? emap[w0 + lane] : 0u;
+                const uint32_t c = static_cast<uint32_t>(__popc(word));
+                uint32_t incl = c;
+    #pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint32_t excl = base + incl - c;
+                const uint32_t want = static_cast<uint32_t>(d);
+                int mine = -1;
+                if (sel < 0 && want >= excl && want < excl + c) {
+                    uint32_t wbits = word;
+                    for (uint32_t j = 0; j < want - excl; ++j) wbits &= wbits - 1u;  // drop the lower set bits
+                    mine = (w0 + lane) * 32 + __ffs(static_cast<int>(wbits)) - 1;
+                }
+                const unsigned who = __ballot_sync(0xffffffffu, mine >= 0);
+                if (who != 0u) sel = __shfl_sync(0xffffffffu, mine, __ffs(static_cast<int>(who)) - 1);
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            // the routed rows that chose it, ascending
+            int cnt = 0;
+            if (sel >= 0) {
+                const unsigned lt = (1u << lane) - 1u;
+                for (int b = 0; b < n_ids; b += 32) {
+                    const int r = b + lane;
+                    const bool hit = r < n_ids && ids_s[r] == static_cast<uint32_t>(sel);
+                    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+                    if (hit) rows_s[cnt + __popc(bal & lt)] = static_cast<uint32_t>(r);
+                    cnt += __popc(bal);
+                }
+            }
+            if (lane == 0) {
+                ctl[2] = static_cast<uint32_t>(sel);
+                ctl[3] = static_cast<uint32_t>(cnt);
             }
         }
-        if (lane == 0) {
-            ctl[2] = static_cast<uint32_t>(sel);
-            ctl[3] = static_cast<uint32_t>(cnt);
-        }
-    }
     }
     tc_fence_before();
     __syncthreads();
