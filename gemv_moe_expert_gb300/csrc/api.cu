@@ -608,7 +608,7 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
         bool tc = (weight_dtype == GBMM_BF16 || weight_dtype == GBMM_F16) && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
                   p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 &&
                   mp.total_rows <= direct_tc_max_ids() && p->n_experts <= static_cast<uint32_t>(direct_tc_max_experts()) &&
-                  direct_tc_block_k() == 64;
+                  p->n < (1u << 31) && p->k < (1u << 31) && direct_tc_block_k() == 64;
         if (tc) {
             PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
             cuuint64_t wdims[3] = {p->k, p->n, p->n_experts};
@@ -655,7 +655,8 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
     CUtensorMap map_w;
     bool tc = weight_dtype == GBMM_BF16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
               p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 && aligned(input, 16) &&
-              p->n_experts <= static_cast<uint32_t>(grouped_tc_max_experts());
+              p->n_experts <= static_cast<uint32_t>(grouped_tc_max_experts()) && p->n < (1u << 31) &&
+              p->k < (1u << 31);
     if (tc) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
         // weights: (k, n, expert), 256 x bk boxes; a box row of bk bf16 is one
@@ -674,7 +675,8 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
     // f16 weights: the Direct route's tensor-core kernel over the map's row lists
     CUtensorMap map_f;
     bool ftc = !tc && weight_dtype == GBMM_F16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
-               p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 && direct_tc_block_k() == 64;
+               p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 && p->n < (1u << 31) && p->k < (1u << 31) &&
+               direct_tc_block_k() == 64;
     if (ftc) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
         cuuint64_t wdims[3] = {p->k, p->n, p->n_experts};
