@@ -94,17 +94,39 @@ def roofline_seconds(wk: dict, peaks: dict, tensor_peak_tf: float) -> float:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle baseline (the oracle as it stands, on a bounded sample)
+# CPU oracle baseline (the oracle as it stands, on the host cores)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_seconds(key: str, w, outputs: int, threads: int) -> tuple[float, int, int]:
-    """Time the oracle on `outputs` sampled elements; returns (seconds,
-    sampled outputs, total outputs)."""
+# Calls the oracle finishes on every output in well under a second; the two
+# large calls (2.7e11 and 2.1e11 multiply-adds) are timed on a sample of their
+# outputs and extrapolated by output count.
+FULL_CPU_KEYS = ("c1", "c2", "c4")
+CPU_SAMPLE = {"c3": 196608, "c5": 196608}   # cpu_baseline leg of our arm
+REF_SAMPLE = {"c3": 32768, "c5": 32768}     # each step of the reference arm
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the record beside the core count."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_call_seconds(key: str, w, outputs: int | None, threads: int) -> tuple[float, int, int]:
+    """Time the oracle on one call: every output when `outputs` is None, else
+    on that many sampled outputs.  Returns (seconds, outputs timed, outputs
+    of the call)."""
     import oracle
     rng = np.random.default_rng(123)
     if key in ("c1", "c2", "c3"):
         total = w.batch * w.m * w.n
-        cnt = min(outputs, total)
+        cnt = total if outputs is None else min(outputs, total)
         idx = rng.choice(total, cnt, replace=False).astype(np.int64) if cnt < total else None
         t0 = time.perf_counter()
         oracle.gemm(w.dtype, w.batch, w.m, w.n, w.k, w.ta, w.tb, w.a.reshape(-1), w.lda,
@@ -112,27 +134,45 @@ def oracle_sample_seconds(key: str, w, outputs: int, threads: int) -> tuple[floa
         return time.perf_counter() - t0, cnt, total
     c = w
     total = c.m * c.top_k * c.n
-    cnt = min(outputs, total)
+    cnt = total if outputs is None else min(outputs, total)
     idx = rng.choice(total, cnt, replace=False).astype(np.int64) if cnt < total else None
     t0 = time.perf_counter()
     oracle.matmul_id(c.wdtype, c.m, c.n, c.k, c.top_k, c.n_experts, c.expert_stride_bytes,
                      c.input_layout, c.w, c.x, c.ids, idx=idx, nthreads=threads)
-    if key == "c5":
+    if c.route == 1:
         oracle.map_distinct(c.m, c.top_k, c.n_experts, c.ids)
     return time.perf_counter() - t0, cnt, total
 
 
-SAMPLE_OUTPUTS = {"c1": 4096, "c2": 11008, "c3": 32768, "c4": 45056, "c5": 32768}
+def cpu_step(workloads: dict, keys, sample: dict, scale: float = 1.0) -> dict:
+    """One pass of the oracle over the step's calls: every output of the small
+    calls, a sample of the large ones (extrapolated by output count)."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    calls, measured, est = {}, 0.0, 0.0
+    for key in keys:
+        n_out = None if key in FULL_CPU_KEYS else max(1, int(sample[key] * scale))
+        secs, cnt, total = oracle_call_seconds(key, workloads[key], n_out, threads)
+        calls[key] = {"seconds": secs, "outputs_timed": cnt, "outputs": total,
+                      "extrapolated": cnt < total, "est_seconds": secs * total / cnt}
+        measured += secs
+        est += secs * total / cnt
+    desc = ", ".join(f"{k}: {v['outputs_timed']}/{v['outputs']} outputs" +
+                     (" (extrapolated)" if v["extrapolated"] else "") for k, v in calls.items())
+    return {"cores": threads, "cpu_model": cpu_model(), "measured_seconds": measured,
+            "est_step_seconds": est, "calls": calls, "sample": desc}
 
 
 def cpu_baseline(workloads: dict, roof_total: float, scale: float = 1.0) -> dict:
-    cb = cpu_baseline_keys(workloads, [k for k in ORDER if k in workloads], roof_total, scale)
+    cb = cpu_step(workloads, [k for k in ORDER if k in workloads], CPU_SAMPLE, scale)
     est_total = cb["est_step_seconds"]
     return {"value": 100.0 * roof_total / est_total, "unit": UNIT, "cores": cb["cores"],
-            "kind": "oracle",
-            "sample": cb["sample"] + f"; full-step time extrapolated by outputs: "
-                                     f"{est_total:.1f} s per step",
-            "est_step_seconds": est_total}
+            "cpu_model": cb["cpu_model"], "kind": "oracle",
+            "sample": cb["sample"] + f"; {cb['measured_seconds']:.1f} s measured, full step "
+                                     f"{est_total:.1f} s with the sampled calls extrapolated",
+            "measured_seconds": cb["measured_seconds"], "est_step_seconds": est_total,
+            "calls": cb["calls"]}
 
 
 # ---------------------------------------------------------------------------
@@ -297,7 +337,8 @@ def run_ours(args) -> None:
 
     keys = [k for k in ORDER if k in args.only]
     peaks, peak_src = load_peaks()
-    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # the timed region is a few tens of milliseconds: the burst tensor rate
+    tensor_peak = peaks["bf16_tflops"]
     workloads = {k: synth.workload(NAMES[k]) for k in keys}
     works = {k: work_of(k, workloads[k]) for k in keys}
     roof = {k: roofline_seconds(works[k], peaks, tensor_peak) for k in keys}
@@ -362,6 +403,12 @@ def run_ours(args) -> None:
     clk = clocks.stop()
     elapsed_ms = start.elapsed_time(end)
     dom_ms_live = sum(e[0].elapsed_time(e[1]) for e in dev_ev) / args.steps
+    # per-step times at no extra cost: every step records one event at the
+    # same place (just before the dominant call), so consecutive ones are one
+    # step apart
+    step_ms = [dev_ev[s][0].elapsed_time(dev_ev[s + 1][0]) for s in range(args.steps - 1)]
+    if keys and keys[0] == dom:
+        step_ms.append(dev_ev[args.steps - 1][0].elapsed_time(end))
     per_call_split = dict(per_call)
     per_call[dom] = dom_ms_live
 
@@ -534,39 +581,54 @@ def run_ours(args) -> None:
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}
     roofline.update({"kernel": dom, "peak_source": peak_src,
-                     "peak_kind": "sustained" if roofline["bound"] == "tensor" else "copy",
+                     "peak_kind": "burst" if roofline["bound"] == "tensor" else "copy",
                      "traffic": TRAFFIC.get(dom)})
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(workloads, roof_total, args.cpu_scale)
 
+    # side measurements outside the step (bounded): the rows beyond the five
+    # workloads, each with its roofline fraction and the clocks seen
+    side = None
+    if not args.no_sweeps and world == 1:
+        side = {}
+        torch.cuda.empty_cache()
+        quick = argparse.Namespace(steps=5, warmup=2)
+        t_side = time.perf_counter()
+        for name, fn in (("skinny_gemv", sweep_skinny), ("route_crossover", sweep_crossover),
+                         ("matmul_id_dtypes", sweep_dtypes), ("ffma_gemm", sweep_ffma)):
+            side[name] = fn(quick, torch, gb, quick=True)
+            torch.cuda.empty_cache()
+        side["seconds"] = time.perf_counter() - t_side
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": statistics.median(step_ms) if step_ms else None,
+        "ms_per_step_min": min(step_ms) if step_ms else None,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16/bf16 in, f32 accumulate (f32 for c1)",
         "data": "synthetic (seeded numpy, seed 0)",
-        "config": {"workload": "hot path: " + " + ".join(NAMES[k] for k in keys),
-                   "calls_per_step": len(keys), "launches_per_step": n_launch,
-                   "l2": "inputs larger than L2 between calls: c5 streams 1.88 GB, each call's "
-                         "inputs evicted by the calls before it",
-                   "parallelism": f"replicas x{world}", "peaks": {k: peaks[k] for k in
-                                                                   ("hbm_gbs", "bf16_tflops",
-                                                                    "bf16_tflops_sustained")
-                                                                   if k in peaks},
-                   "roofline_ms_per_step": roof_total * 1e3, "calls": calls,
-                   "calls_timing": (f"{dom}: events around its launches in every timed step; the other "
-                                    f"calls: an instrumented pass of {split_steps} steps with an event "
-                                    "between every two launches (those events are kept out of the timed "
-                                    "steps)"),
-                   "calls_split_ms": per_call_split,
-                   "calls_steady": steady,
-                   "calls_steady_timing": ("each call alone, 50 launches back to back between two events, "
-                                           "inputs rotated over input_copies device copies so that every "
-                                           "launch reads them from HBM (not part of the step)"),
-                   "c5_single_rounding_option": single},
+        "config": step_config(keys, peaks),
+        "roofline_ms_per_step": roof_total * 1e3, "launches_per_step": n_launch,
+        "step_times_ms": step_ms,
+        "step_times_timing": ("one event per timed step just before the dominant call: consecutive events are "
+                              "one step apart (no extra event in the step)"),
+        "calls": calls,
+        "calls_timing": (f"{dom}: events around its launches in every timed step; the other "
+                         f"calls: an instrumented pass of {split_steps} steps with an event "
+                         "between every two launches (those events are kept out of the timed "
+                         "steps)"),
+        "calls_split_ms": per_call_split,
+        "calls_steady": steady,
+        "calls_steady_timing": ("each call alone, 50 launches back to back between two events, "
+                                "inputs rotated over input_copies device copies so that every "
+                                "launch reads them from HBM (not part of the step)"),
+        "c5_single_rounding_option": single,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk, "wall_s_timed": wall,
+        "side_sweeps": side,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -584,7 +646,22 @@ TRAFFIC: dict = {"c5": 2_209_137_464}
 # reference arm: the CPU oracle, as it stands, on the machine's host cores
 # ---------------------------------------------------------------------------
 
+def step_config(keys, peaks) -> dict:
+    """The workload description both arms print (static: no measured values)."""
+    return {"workload": "hot path: " + " + ".join(NAMES[k] for k in keys),
+            "calls_per_step": len(keys),
+            "l2": "inputs larger than L2 between calls: c5 streams 1.88 GB, each call's inputs "
+                  "evicted by the calls before it",
+            "parallelism": "replicas (one process per GPU, no exchange step)",
+            "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in peaks}}
+
+
 def run_reference(args) -> None:
+    """The oracle as it stands on the host cores.  Each step is one bounded
+    sample of the step's workload: every output of c1, c2 and c4, a sample of
+    the outputs of c3 and c5; `ms_per_step` is the time those steps took,
+    `value` the metric with the two sampled calls extrapolated to all their
+    outputs."""
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
@@ -592,108 +669,42 @@ def run_reference(args) -> None:
     oracle.build()
     keys = [k for k in ORDER if k in args.only]
     peaks, _ = load_peaks()
-    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    tensor_peak = peaks["bf16_tflops"]
     workloads = {k: synth.workload(NAMES[k]) for k in keys}
     roof_total = sum(roofline_seconds(work_of(k, workloads[k]), peaks, tensor_peak) for k in keys)
-    scale = args.cpu_scale * 0.25
+    scale = args.cpu_scale
     for _ in range(args.warmup):
-        cpu_baseline_keys(workloads, keys, roof_total, scale * 0.05)
-    ests = []
+        cpu_step(workloads, keys, REF_SAMPLE, scale)
+    steps = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        cb = cpu_baseline_keys(workloads, keys, roof_total, scale)
-        ests.append(cb["est_step_seconds"])
+        steps.append(cpu_step(workloads, keys, REF_SAMPLE, scale))
     wall = time.perf_counter() - t0
-    est = statistics.mean(ests)
+    est = statistics.mean(st["est_step_seconds"] for st in steps)
     value = 100.0 * roof_total / est
-    cpu = {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
-           "sample": cb["sample"]}
+    last = steps[-1]
+    cpu = {"value": value, "unit": UNIT, "cores": last["cores"], "cpu_model": last["cpu_model"],
+           "kind": "oracle", "sample": last["sample"] + " per step",
+           "measured_seconds_per_step": wall / max(1, args.steps),
+           "est_full_step_seconds": est, "calls": last["calls"]}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (oracle)",
             "data": "synthetic (seeded numpy, seed 0)", "impl": "reference",
-            "config": {"workload": "hot path: " + " + ".join(NAMES[k] for k in keys),
-                       "note": "the CPU oracle timed on sampled outputs of each call and "
-                               "extrapolated to the full step"},
+            "config": step_config(keys, peaks),
+            "timing": ("ms_per_step: wall time of each timed step, one bounded sample of the workload (every "
+                       "output of the small calls, sampled outputs of the large ones); value: the metric for "
+                       f"the full step, the sampled calls extrapolated by output count ({est:.1f} s per full "
+                       "step)"),
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s_timed": wall}
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_keys(workloads, keys, roof_total, scale):
-    import oracle
-    oracle.build()
-    threads = os.cpu_count() or 1
-    est_total, parts = 0.0, []
-    for key in keys:
-        n_out = max(1, int(SAMPLE_OUTPUTS[key] * scale))
-        secs, cnt, total = oracle_sample_seconds(key, workloads[key], n_out, threads)
-        est_total += secs * total / cnt
-        parts.append(f"{key}:{cnt}/{total}")
-    return {"cores": threads, "est_step_seconds": est_total,
-            "sample": "sampled outputs per call (" + ", ".join(parts) + ")"}
-
-
 # ---------------------------------------------------------------------------
-# Direct vs GroupedPrefill crossover (the caller picks the route)
+# side sweeps: the rows beyond the five workloads (each call timed alone)
 # ---------------------------------------------------------------------------
-
-def run_crossover(args) -> None:
-    """Both expert-ID routes on the grouped workload's expert stack (128
-    experts of bf16 [1536, 4096], top-8 Zipf(1.1) ids, SharedPerToken f32 x)
-    for m = 1 .. 512 tokens, each call timed alone after an L2 flush (median of
-    --steps calls).  Prints one JSON line with the table and the first m at
-    which GroupedPrefill is faster, for callers that choose the route."""
-    import torch
-    from gemv_moe_expert_gb300 import binding as gb
-    from gemv_moe_expert_gb300 import build
-    build.build()
-    gb.load()
-    E, top_k, k, n = 128, 8, 4096, 1536
-    stride = n * k * 2
-    g = torch.Generator(device="cuda").manual_seed(0)
-    w = (torch.randn(E * n * k, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    rows = []
-    for m in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
-        ids_h = synth.distinct_ids(m, top_k, E, seed=m, zipf_s=1.1)
-        ids = torch.from_numpy(ids_h.view(np.int32).reshape(-1).copy()).cuda()
-        x = torch.randn(m * k, device="cuda", generator=g)
-        out = torch.empty(m * top_k * n, device="cuda")
-        entry = {"m": m, "distinct_experts": int(len(np.unique(ids_h)))}
-        for route, name in ((gb.ROUTE_DIRECT, "direct_us"), (gb.ROUTE_GROUPED_PREFILL, "grouped_us")):
-            p = gb.make_params(m, n, k, top_k, E, stride, 0, 0, route)
-            st, cap = gb.gbmm_matmul_id_capability("bf16", p)
-            gb.check(st)
-            sc = None
-            if route == gb.ROUTE_GROUPED_PREFILL:
-                cnt = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device="cuda")
-                rr = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device="cuda")
-                sc = gb.make_scratch(cnt, cap.expert_counts_bytes, rr, cap.routed_rows_bytes, E, m)
-
-            def call():
-                gb.check(gb.gbmm_matmul_id(p, "bf16", w, w.numel() * 2, x, x.numel() * 4, ids, ids.numel() * 4,
-                                           out, out.numel() * 4, sc)[0])
-            for _ in range(args.warmup):
-                call()
-            torch.cuda.synchronize()
-            ts = []
-            for _ in range(args.steps):
-                flush.fill_(1)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                call()
-                e1.record()
-                torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1) * 1e3)
-            entry[name] = statistics.median(ts)
-        rows.append(entry)
-    cross = next((r["m"] for r in rows if r["grouped_us"] < r["direct_us"]), None)
-    print(json.dumps({"sweep": "matmul_id route crossover", "experts": E, "top_k": top_k, "k": k, "n": n,
-                      "weights": "bf16", "ids": "top-8 distinct Zipf(1.1)", "rows": rows,
-                      "grouped_faster_from_m": cross}), flush=True)
-
 
 def _time_alone(call, torch, flush, steps, warmup):
     """Median of `steps` calls, each timed with CUDA events after an L2 flush.
@@ -717,153 +728,235 @@ def _time_alone(call, torch, flush, steps, warmup):
     return statistics.median(ts)
 
 
-def run_ffma(args) -> None:
-    """The f32 GEMM on the FFMA pipe at compute-bound sizes (f32 has no
-    tensor-core route here): 4096^3 for every transpose pair and 2048^3 nt,
-    each call timed alone after an L2 flush, with its fraction of the FFMA
-    peak (152 SMs x 128 lanes x 2 flops at the sampled SM clock)."""
+def _with_clocks(fn):
+    """Run fn() with the SM clocks sampled; returns (result, clocks)."""
     import torch
-    from gemv_moe_expert_gb300 import binding as gb
-    from gemv_moe_expert_gb300 import build
-    build.build()
-    gb.load()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    try:
+        res = fn()
+    finally:
+        clk = clocks.stop()
+    return res, clk
+
+
+def sweep_crossover(args, torch, gb, quick=False) -> dict:
+    """Both expert-ID routes on the grouped workload's expert stack (128
+    experts of bf16 [1536, 4096], top-8 Zipf(1.1) ids, SharedPerToken f32 x)
+    over m tokens, each call timed alone after an L2 flush (median of
+    args.steps calls), with the first m at which GroupedPrefill is faster, for
+    callers that choose the route."""
+    peaks, _ = load_peaks()
+    E, top_k, k, n = 128, 8, 4096, 1536
+    stride = n * k * 2
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w = (torch.randn(E * n * k, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ms = (1, 8, 32, 64, 512) if quick else (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)
+
+    def run():
+        rows = []
+        for m in ms:
+            ids_h = synth.distinct_ids(m, top_k, E, seed=m, zipf_s=1.1)
+            ids = torch.from_numpy(ids_h.view(np.int32).reshape(-1).copy()).cuda()
+            x = torch.randn(m * k, device="cuda", generator=g)
+            out = torch.empty(m * top_k * n, device="cuda")
+            distinct = int(len(np.unique(ids_h)))
+            bytes_ = distinct * stride + x.numel() * 4 + ids.numel() * 4 + out.numel() * 4
+            flops = 2 * m * top_k * n * k
+            roof_us = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+            entry = {"m": m, "distinct_experts": distinct, "roofline_us": roof_us}
+            for route, name in ((gb.ROUTE_DIRECT, "direct"), (gb.ROUTE_GROUPED_PREFILL, "grouped")):
+                p = gb.make_params(m, n, k, top_k, E, stride, 0, 0, route)
+                st, cap = gb.gbmm_matmul_id_capability("bf16", p)
+                gb.check(st)
+                sc = None
+                if route == gb.ROUTE_GROUPED_PREFILL:
+                    cnt = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device="cuda")
+                    rr = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device="cuda")
+                    sc = gb.make_scratch(cnt, cap.expert_counts_bytes, rr, cap.routed_rows_bytes, E, m)
+
+                def call():
+                    gb.check(gb.gbmm_matmul_id(p, "bf16", w, w.numel() * 2, x, x.numel() * 4, ids,
+                                               ids.numel() * 4, out, out.numel() * 4, sc)[0])
+                us = _time_alone(call, torch, flush, args.steps, args.warmup)
+                entry[name + "_us"] = us
+                entry[name + "_frac_of_roofline"] = roof_us / us
+                entry[name + "_kernel"] = gb.gbmm_test_last_kernel()
+            rows.append(entry)
+        return rows
+
+    rows, clk = _with_clocks(run)
+    cross = next((r["m"] for r in rows if r["grouped_us"] < r["direct_us"]), None)
+    return {"sweep": "matmul_id route crossover", "experts": E, "top_k": top_k, "k": k, "n": n,
+            "weights": "bf16", "ids": "top-8 distinct Zipf(1.1)",
+            "timing": "each call alone after an L2 flush, median of %d" % args.steps,
+            "roofline": "max(bytes of the distinct experts read + x + ids + out / HBM peak, flops / burst "
+                        "bf16 peak)", "rows": rows, "grouped_faster_from_m": cross, "clocks": clk}
+
+
+def sweep_ffma(args, torch, gb, quick=False) -> dict:
+    """The f32 GEMM on the FFMA pipe at compute-bound sizes (f32 has no
+    tensor-core route here), each call timed alone after an L2 flush, with its
+    fraction of the FFMA peak (152 SMs x 128 lanes x 2 flops at the sampled SM
+    clock)."""
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(0)
-    rows = []
-    for (m, n, k, ta, tb) in [(4096, 4096, 4096, 0, 0), (4096, 4096, 4096, 0, 1), (4096, 4096, 4096, 1, 0),
-                              (4096, 4096, 4096, 1, 1), (2048, 2048, 2048, 0, 1)]:
-        a = torch.randn(m * k, device="cuda", generator=g) / np.sqrt(k)
-        b = torch.randn(n * k, device="cuda", generator=g)
-        c = torch.empty(m * n, device="cuda")
-        lda, ldb = (m if ta else k), (k if tb else n)
+    shapes = [(4096, 4096, 4096, 0, 0), (4096, 4096, 4096, 0, 1)]
+    if not quick:
+        shapes += [(4096, 4096, 4096, 1, 0), (4096, 4096, 4096, 1, 1), (2048, 2048, 2048, 0, 1)]
 
-        def call():
-            gb.check(gb.gbmm_gemm("f32", 1, m, n, k, ta, tb, a, 0, lda, m * k, b, 0, ldb, n * k, c, 0, n, m * n))
+    def run():
+        rows = []
+        for (m, n, k, ta, tb) in shapes:
+            a = torch.randn(m * k, device="cuda", generator=g) / np.sqrt(k)
+            b = torch.randn(n * k, device="cuda", generator=g)
+            c = torch.empty(m * n, device="cuda")
+            lda, ldb = (m if ta else k), (k if tb else n)
 
-        clocks = ClockSampler(0)
-        clocks.start()
-        us = _time_alone(call, torch, flush, args.steps, args.warmup)
-        clk = clocks.stop() or {}
-        peak = ffma_peak_tflops(clk.get("sm_mhz") or 2070.0)
-        tflops = 2 * m * n * k / (us * 1e-6) / 1e12
-        rows.append({"m": m, "n": n, "k": k, "ta": ta, "tb": tb, "us": us, "tflops": tflops,
-                     "ffma_peak_tflops": peak, "frac_of_ffma_peak": tflops / peak,
-                     "kernel": gb.gbmm_test_last_kernel(), "sm_mhz": clk.get("sm_mhz")})
-        del a, b, c
-    print(json.dumps({"sweep": "f32 GEMM on the FFMA pipe", "timing": "each call alone after an L2 flush, "
-                      "median of --steps", "rows": rows}), flush=True)
+            def call():
+                gb.check(gb.gbmm_gemm("f32", 1, m, n, k, ta, tb, a, 0, lda, m * k, b, 0, ldb, n * k, c, 0, n,
+                                      m * n))
+            us = _time_alone(call, torch, flush, args.steps, args.warmup)
+            rows.append({"m": m, "n": n, "k": k, "ta": ta, "tb": tb, "us": us,
+                         "tflops": 2 * m * n * k / (us * 1e-6) / 1e12, "kernel": gb.gbmm_test_last_kernel()})
+            del a, b, c
+        return rows
+
+    rows, clk = _with_clocks(run)
+    peak = ffma_peak_tflops((clk or {}).get("sm_mhz") or 2070.0)
+    for r in rows:
+        r["ffma_peak_tflops"] = peak
+        r["frac_of_ffma_peak"] = r["tflops"] / peak
+    return {"sweep": "f32 GEMM on the FFMA pipe", "timing": "each call alone after an L2 flush, median of "
+            "%d" % args.steps, "rows": rows, "clocks": clk}
 
 
-def run_skinny(args) -> None:
+def sweep_skinny(args, torch, gb, quick=False) -> dict:
     """The decode GEMV y[m, n] = x[m, k] W[n, k]^T (B stored [n, k], batch 1)
-    for m = 1 .. 15 tokens on the decode workload's shape (n 11008, k 4096), f16
-    and bf16 (and f32 at m = 1): each call timed alone after an L2 flush, with
-    the kernel that served it and its fraction of the HBM roofline (bytes of W,
-    x and y)."""
-    import torch
-    from gemv_moe_expert_gb300 import binding as gb
-    from gemv_moe_expert_gb300 import build
-    build.build()
-    gb.load()
+    for m = 1 .. 15 tokens on the decode workload's shape (n 11008, k 4096),
+    f16 and bf16 (and f32 at m = 1), plus the other GEMV orientations of the
+    same f16 matrix: each call timed alone after an L2 flush, with the kernel
+    that served it and its fraction of the HBM roofline (bytes of W, x and
+    y)."""
     peaks, _ = load_peaks()
     n, k = 11008, 4096
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(0)
-    rows = []
-    for dt, tdt, ms in (("f16", torch.float16, (1, 2, 3, 4, 6, 8, 12, 15)),
-                        ("bf16", torch.bfloat16, (1, 2, 4, 8, 15)), ("f32", torch.float32, (1,))):
-        size = synth.ITEMSIZE[dt]
-        w = (torch.randn(n * k, device="cuda", generator=g) * 0.02).to(tdt)
-        for m in ms:
-            x = torch.randn(m * k, device="cuda", generator=g).to(tdt)
-            y = torch.empty(m * n, device="cuda", dtype=tdt)
+    sets = ((("f16", torch.float16, (1, 2, 4, 8, 15)), ("bf16", torch.bfloat16, (1, 8)),
+             ("f32", torch.float32, (1,))) if quick else
+            (("f16", torch.float16, (1, 2, 3, 4, 6, 8, 12, 15)), ("bf16", torch.bfloat16, (1, 2, 4, 8, 15)),
+             ("f32", torch.float32, (1,))))
+
+    def run():
+        rows = []
+        for dt, tdt, ms in sets:
+            size = synth.ITEMSIZE[dt]
+            w = (torch.randn(n * k, device="cuda", generator=g) * 0.02).to(tdt)
+            for m in ms:
+                x = torch.randn(m * k, device="cuda", generator=g).to(tdt)
+                y = torch.empty(m * n, device="cuda", dtype=tdt)
+
+                def call():
+                    gb.check(gb.gbmm_gemm(dt, 1, m, n, k, 0, 1, x, 0, k, m * k, w, 0, k, n * k, y, 0, n, m * n))
+                us = _time_alone(call, torch, flush, args.steps, args.warmup)
+                bytes_ = (n * k + m * k + m * n) * size
+                rows.append({"dtype": dt, "m": m, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
+                             "frac_of_hbm": bytes_ / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6),
+                             "kernel": gb.gbmm_test_last_kernel()})
+        # the vector times B stored [k, n] (outputs contiguous in the matrix
+        # rows), and n == 1 with A stored [m, k] or [k, m]
+        w = (torch.randn(n * k, device="cuda", generator=g) * 0.02).half()
+        x = torch.randn(k, device="cuda", generator=g).half()
+        y = torch.empty(n, device="cuda", dtype=torch.float16)
+        for label, args_ in (("m1_B_stored_kn", (1, n, k, 0, 0, x, k, k, w, n, n * k, y, n, n)),
+                             ("n1_A_stored_mk", (n, 1, k, 0, 1, w, k, n * k, x, k, k, y, 1, n)),
+                             ("n1_A_stored_km", (n, 1, k, 1, 1, w, n, n * k, x, k, k, y, 1, n))):
+            mm, nn, kk, ta, tb, a_, lda, sa, b_, ldb, sb, c_, ldc, sc = args_
 
             def call():
-                gb.check(gb.gbmm_gemm(dt, 1, m, n, k, 0, 1, x, 0, k, m * k, w, 0, k, n * k, y, 0, n, m * n))
+                gb.check(gb.gbmm_gemv("f16", 1, mm, nn, kk, ta, tb, a_, 0, lda, sa, b_, 0, ldb, sb, c_, 0, ldc,
+                                      sc))
             us = _time_alone(call, torch, flush, args.steps, args.warmup)
-            bytes_ = (n * k + m * k + m * n) * size
-            rows.append({"dtype": dt, "m": m, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
+            bytes_ = (n * k + k + n) * 2
+            rows.append({"dtype": "f16", "orientation": label, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
                          "frac_of_hbm": bytes_ / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6),
                          "kernel": gb.gbmm_test_last_kernel()})
-    # the other GEMV orientations on the same 11008 x 4096 f16 matrix: the vector times B stored [k, n]
-    # (outputs contiguous in the matrix rows), and n == 1 with A stored [m, k] or [k, m]
-    w = (torch.randn(n * k, device="cuda", generator=g) * 0.02).half()
-    x = torch.randn(k, device="cuda", generator=g).half()
-    y = torch.empty(n, device="cuda", dtype=torch.float16)
-    for label, args_ in (("m1_B_stored_kn", (1, n, k, 0, 0, x, k, k, w, n, n * k, y, n, n)),
-                         ("n1_A_stored_mk", (n, 1, k, 0, 1, w, k, n * k, x, k, k, y, 1, n)),
-                         ("n1_A_stored_km", (n, 1, k, 1, 1, w, n, n * k, x, k, k, y, 1, n))):
-        mm, nn, kk, ta, tb, a_, lda, sa, b_, ldb, sb, c_, ldc, sc = args_
+        return rows
 
-        def call():
-            gb.check(gb.gbmm_gemv("f16", 1, mm, nn, kk, ta, tb, a_, 0, lda, sa, b_, 0, ldb, sb, c_, 0, ldc, sc))
-        us = _time_alone(call, torch, flush, args.steps, args.warmup)
-        bytes_ = (n * k + k + n) * 2
-        rows.append({"dtype": "f16", "orientation": label, "us": us, "gbs": bytes_ / (us * 1e-6) / 1e9,
-                     "frac_of_hbm": bytes_ / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6),
-                     "kernel": gb.gbmm_test_last_kernel()})
-    print(json.dumps({"sweep": "skinny decode GEMV", "n": n, "k": k, "layout": "B stored [n, k], batch 1 "
-                      "(plus the rows with an orientation)",
-                      "timing": "each call alone after an L2 flush, median of --steps", "rows": rows}), flush=True)
+    rows, clk = _with_clocks(run)
+    return {"sweep": "skinny decode GEMV", "n": n, "k": k, "layout": "B stored [n, k], batch 1 (plus the rows "
+            "with an orientation)", "timing": "each call alone after an L2 flush, median of %d" % args.steps,
+            "rows": rows, "clocks": clk}
 
 
-def run_dtypes(args) -> None:
+def sweep_dtypes(args, torch, gb, quick=False) -> dict:
     """The expert-ID matmul for every weight dtype, input layout and id
     multiplicity the capability accepts: Direct on a decode shape (4 tokens x
     top-8 of 64 experts, k 2048, n 1408) and GroupedPrefill on a prefill shape
     (512 tokens, same experts), each call timed alone after an L2 flush, with
     its fraction of the roofline (HBM bytes of the experts the call reads, x,
-    ids and out; tensor flops at the bf16 peak for 16-bit weights, the FFMA
-    peak for f32 weights)."""
+    ids and out; tensor flops at the burst bf16 peak for 16-bit weights, the
+    FFMA peak for f32 weights)."""
+    peaks, _ = load_peaks()
+    tensor_peak = peaks["bf16_tflops"]
+    E, top_k, k, n = 64, 8, 2048, 1408
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(0)
+
+    def run():
+        rows = []
+        for wdt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16), ("f32", torch.float32)):
+            size = synth.ITEMSIZE[wdt]
+            w = (torch.randn(E * n * k, device="cuda", generator=g) * 0.02).to(tdt)
+            cases = [("direct", 4, 0, 0), ("direct", 4, 1, 0), ("direct", 4, 0, 1),
+                     ("grouped", 512, 0, 0), ("grouped", 512, 1, 0)]
+            for route_name, m, layout, mult in cases:
+                route = gb.ROUTE_DIRECT if route_name == "direct" else gb.ROUTE_GROUPED_PREFILL
+                ids_h = (synth.repeat_ids(m, top_k, E, seed=m) if mult else synth.distinct_ids(m, top_k, E, seed=m))
+                ids = torch.from_numpy(ids_h.view(np.int32).reshape(-1).copy()).cuda()
+                x_rows = m if layout == 0 else m * top_k
+                x = torch.randn(x_rows * k, device="cuda", generator=g)
+                out = torch.empty(m * top_k * n, device="cuda")
+                p = gb.make_params(m, n, k, top_k, E, n * k * size, layout, mult, route)
+                st, cap = gb.gbmm_matmul_id_capability(wdt, p)
+                gb.check(st)
+                sc = None
+                if route == gb.ROUTE_GROUPED_PREFILL:
+                    cnt = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device="cuda")
+                    rr = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device="cuda")
+                    sc = gb.make_scratch(cnt, cap.expert_counts_bytes, rr, cap.routed_rows_bytes, E, m)
+
+                def call():
+                    gb.check(gb.gbmm_matmul_id(p, wdt, w, w.numel() * size, x, x.numel() * 4, ids,
+                                               ids.numel() * 4, out, out.numel() * 4, sc)[0])
+                us = _time_alone(call, torch, flush, args.steps, args.warmup)
+                distinct = int(len(np.unique(ids_h)))
+                bytes_ = distinct * n * k * size + x.numel() * 4 + ids.numel() * 4 + out.numel() * 4
+                flops = 2 * m * top_k * n * k
+                peak_tf = ffma_peak_tflops() if wdt == "f32" else tensor_peak
+                roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12))
+                rows.append({"weights": wdt, "route": route_name, "m": m,
+                             "layout": "Slotted" if layout else "SharedPerToken",
+                             "ids": "MayRepeat" if mult else "DistinctPerToken", "distinct_experts": distinct,
+                             "us": us, "roofline_us": roof * 1e6, "frac_of_roofline": roof / (us * 1e-6),
+                             "kernel": gb.gbmm_test_last_kernel()})
+            del w
+        return rows
+
+    rows, clk = _with_clocks(run)
+    return {"sweep": "matmul_id weight dtypes, layouts and multiplicity", "experts": E, "top_k": top_k,
+            "k": k, "n": n, "timing": "each call alone after an L2 flush, median of %d" % args.steps,
+            "rows": rows, "clocks": clk}
+
+
+def run_sweep(args, fn) -> None:
     import torch
     from gemv_moe_expert_gb300 import binding as gb
     from gemv_moe_expert_gb300 import build
     build.build()
     gb.load()
-    peaks, _ = load_peaks()
-    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    E, top_k, k, n = 64, 8, 2048, 1408
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    g = torch.Generator(device="cuda").manual_seed(0)
-    rows = []
-    for wdt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16), ("f32", torch.float32)):
-        size = synth.ITEMSIZE[wdt]
-        w = (torch.randn(E * n * k, device="cuda", generator=g) * 0.02).to(tdt)
-        cases = [("direct", 4, 0, 0), ("direct", 4, 1, 0), ("direct", 4, 0, 1),
-                 ("grouped", 512, 0, 0), ("grouped", 512, 1, 0)]
-        for route_name, m, layout, mult in cases:
-            route = gb.ROUTE_DIRECT if route_name == "direct" else gb.ROUTE_GROUPED_PREFILL
-            ids_h = (synth.repeat_ids(m, top_k, E, seed=m) if mult else synth.distinct_ids(m, top_k, E, seed=m))
-            ids = torch.from_numpy(ids_h.view(np.int32).reshape(-1).copy()).cuda()
-            x_rows = m if layout == 0 else m * top_k
-            x = torch.randn(x_rows * k, device="cuda", generator=g)
-            out = torch.empty(m * top_k * n, device="cuda")
-            p = gb.make_params(m, n, k, top_k, E, n * k * size, layout, mult, route)
-            st, cap = gb.gbmm_matmul_id_capability(wdt, p)
-            gb.check(st)
-            sc = None
-            if route == gb.ROUTE_GROUPED_PREFILL:
-                cnt = torch.empty(cap.expert_counts_bytes, dtype=torch.uint8, device="cuda")
-                rr = torch.empty(cap.routed_rows_bytes, dtype=torch.uint8, device="cuda")
-                sc = gb.make_scratch(cnt, cap.expert_counts_bytes, rr, cap.routed_rows_bytes, E, m)
-
-            def call():
-                gb.check(gb.gbmm_matmul_id(p, wdt, w, w.numel() * size, x, x.numel() * 4, ids, ids.numel() * 4,
-                                           out, out.numel() * 4, sc)[0])
-            us = _time_alone(call, torch, flush, args.steps, args.warmup)
-            distinct = int(len(np.unique(ids_h)))
-            bytes_ = distinct * n * k * size + x.numel() * 4 + ids.numel() * 4 + out.numel() * 4
-            flops = 2 * m * top_k * n * k
-            peak_tf = ffma_peak_tflops() if wdt == "f32" else tensor_peak
-            roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12))
-            rows.append({"weights": wdt, "route": route_name, "m": m,
-                         "layout": "Slotted" if layout else "SharedPerToken",
-                         "ids": "MayRepeat" if mult else "DistinctPerToken", "distinct_experts": distinct,
-                         "us": us, "roofline_us": roof * 1e6, "frac_of_roofline": roof / (us * 1e-6),
-                         "kernel": gb.gbmm_test_last_kernel()})
-    print(json.dumps({"sweep": "matmul_id weight dtypes, layouts and multiplicity", "experts": E,
-                      "top_k": top_k, "k": k, "n": n, "timing": "each call alone after an L2 flush, median of --steps",
-                      "rows": rows}), flush=True)
+    print(json.dumps(fn(args, torch, gb, quick=False)), flush=True)
 
 
 def main():
@@ -878,6 +971,8 @@ def main():
     ap.add_argument("--cpu-scale", type=float, default=1.0)
     ap.add_argument("--no-options", action="store_true", help="skip the opt-in mode side timings")
     ap.add_argument("--no-steady", action="store_true", help="skip the per-call back-to-back timings")
+    ap.add_argument("--no-sweeps", action="store_true",
+                    help="skip the side sweeps (skinny GEMV, route crossover, matmul_id dtypes, FFMA GEMM)")
     ap.add_argument("--sweep", choices=["crossover", "skinny", "dtypes", "ffma"], default=None,
                     help="instead of the step: crossover = Direct against GroupedPrefill for m = 1..512; "
                          "skinny = the decode GEMV for m = 1..15; dtypes = the expert-ID matmul for every "
@@ -886,14 +981,9 @@ def main():
     args.only = [k.strip() for k in args.only.split(",") if k.strip()]
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.sweep == "crossover":
-        run_crossover(args)
-    elif args.sweep == "skinny":
-        run_skinny(args)
-    elif args.sweep == "dtypes":
-        run_dtypes(args)
-    elif args.sweep == "ffma":
-        run_ffma(args)
+    if args.sweep is not None:
+        run_sweep(args, {"crossover": sweep_crossover, "skinny": sweep_skinny, "dtypes": sweep_dtypes,
+                         "ffma": sweep_ffma}[args.sweep])
     elif args.impl == "reference":
         run_reference(args)
     else:

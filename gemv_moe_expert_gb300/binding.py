@@ -43,7 +43,7 @@ EXPORTS = (
     "gbmm_matmul_id", "gbmm_last_error", "gbmm_status_string", "gbmm_abi_version",
     "gbmm_device_error", "gbmm_test_inject_kernel_failure", "gbmm_test_launch_count",
     "gbmm_test_reset_launch_count", "gbmm_test_last_kernel", "gbmm_test_bounded_wait",
-    "gbmm_matmul_id_static_scratch",
+    "gbmm_matmul_id_static_scratch", "gbmm_test_static_scratch_copy",
 )
 
 # n_experts * m * 4 bytes of routed rows fit the fixed scratch of
@@ -134,6 +134,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                       vp, u64, vp, u64, vp, u64, vp,
                                                       ctypes.POINTER(MatmulIdReceipt)]
         lib.gbmm_matmul_id_static_scratch.restype = i32
+        lib.gbmm_test_static_scratch_copy.argtypes = [vp, u64, vp]
+        lib.gbmm_test_static_scratch_copy.restype = i32
         _lib = lib
         return lib
 
@@ -282,6 +284,11 @@ def gbmm_test_bounded_wait(limit_ns: int, stream=None):
     code = ctypes.c_uint32(0)
     st = load().gbmm_test_bounded_wait(limit_ns, _stream(stream), ctypes.byref(code))
     return st, code.value
+
+
+def gbmm_test_static_scratch_copy(dst, nbytes: int, stream=None) -> int:
+    """Copy the first `nbytes` of the static scratch array into device buffer `dst`."""
+    return load().gbmm_test_static_scratch_copy(_ptr(dst), nbytes, _stream(stream))
 
 
 class GbmmError(RuntimeError):

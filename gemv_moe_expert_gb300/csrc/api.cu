@@ -41,9 +41,15 @@ gbmm_status fail(gbmm_status s, const char *fmt, ...) {
     return s;
 }
 
-// A kernel is "resolved" unless a test injected a one-shot failure for it.
+// A kernel is "resolved" unless a test injected a failure for it: a one-shot
+// failure for one kernel name, or, with the name "*", a failure of every
+// kernel until the injection is cleared.
 bool resolve(const char *name) {
     std::lock_guard<std::mutex> g(g_inject_mu);
+    if (g_inject_name == "*") {
+        t_last_error = std::string("kernel unavailable: ") + name + " (every launch blocked)";
+        return false;
+    }
     if (!g_inject_name.empty() && g_inject_name == name) {
         g_inject_name.clear();
         t_last_error = std::string("kernel unavailable: ") + name;

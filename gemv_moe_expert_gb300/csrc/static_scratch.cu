@@ -36,7 +36,10 @@ uint32_t *g_addr[64] = {nullptr};
 
 // Device address of g_static_scratch on the current device, looked up once
 // per device.  In host code the array's name only stands for the device
-// symbol; the kernels must be given the address the runtime reports.
+// symbol; the kernels must be given the address the runtime reports.  The
+// first lookup on a device also loads this part of the library there (lazy
+// module loading), which reserves the array; the cached address is only
+// valid while the device's primary context lives (not across a device reset).
 gbmm_status scratch_address(uint32_t **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -105,4 +108,18 @@ extern "C" gbmm_status gbmm_matmul_id_static_scratch(const gbmm_matmul_id_params
     s.max_tokens = p->m;
     return gbmm_matmul_id(p, weight_dtype, weights, weights_bytes, input, input_bytes, ids, ids_bytes,
                           out, out_bytes, &s, stream, receipt);
+}
+
+extern "C" gbmm_status gbmm_test_static_scratch_copy(void *dst, uint64_t bytes, gbmm_stream stream) {
+    if (dst == nullptr || bytes > kScratchWords * 4)
+        return static_cast<gbmm_status>(gbmm::record_error(
+            GBMM_ERR_INVALID_ARGUMENT, "gbmm_test_static_scratch_copy: null destination or more bytes than the array"));
+    uint32_t *base = nullptr;
+    gbmm_status st = scratch_address(&base);
+    if (st != GBMM_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(dst, base, bytes, cudaMemcpyDeviceToDevice,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return static_cast<gbmm_status>(gbmm::record_error(GBMM_ERR_CUDA, cudaGetErrorString(e)));
+    return GBMM_OK;
 }

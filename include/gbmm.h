@@ -316,8 +316,15 @@ GBMM_API gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype w
  * them -- race on the array and corrupt each other's results; order them.
  *
  * Set-up: the first call on each device (that device current) looks up the
- * array's device address with cudaGetSymbolAddress and caches it; make that
- * first call before any stream capture on the device.
+ * array's device address with cudaGetSymbolAddress and caches it.  With the
+ * CUDA runtime's lazy module loading (the default) that lookup is also what
+ * loads the array onto the device: a one-time device allocation made by the
+ * CUDA runtime, not by this library.  So make one call per device as a
+ * warm-up, before serving starts and before any stream capture on it.  The
+ * cached address belongs to the device's current context: after
+ * cudaDeviceReset (or any reset of the primary context) the array may live
+ * at another address, and this entry point must not be called again in that
+ * process.
  */
 #define GBMM_STATIC_SCRATCH_ROUTED_ROWS_BYTES (4u << 20)
 GBMM_API gbmm_status gbmm_matmul_id_static_scratch(const gbmm_matmul_id_params *p,
@@ -360,6 +367,9 @@ GBMM_API gbmm_status gbmm_device_error(gbmm_stream stream, uint32_t *code);
 
 /* Makes the next resolution of kernel `name` fail (one shot), like [P2]'s
  * `KernelRegistry::inject_next_pipeline_lookup_failure`.  NULL clears it.
+ * The name "*" makes every resolution fail until cleared: a call that passes
+ * validation then returns GBMM_ERR_KERNEL_UNAVAILABLE with nothing launched
+ * (tests that hand the library addresses no kernel may touch use it).
  * Kernel names: "gbmm_gemv_rowdot", "gbmm_gemv_coldot", "gbmm_gemv_tc", "gbmm_gemm_simt",
  * "gbmm_gemm_tc", "gbmm_fill_zero", "gbmm_matmul_id_direct",
  * "gbmm_matmul_id_map", "gbmm_matmul_id_grouped". */
@@ -386,6 +396,18 @@ GBMM_API const char *gbmm_test_last_kernel(void);
  * set).  Exercises the timeout path without faulting or hanging the GPU.
  */
 GBMM_API gbmm_status gbmm_test_bounded_wait(uint64_t limit_ns, gbmm_stream stream, uint32_t *code);
+
+/*
+ * gbmm_test_static_scratch_copy -- enqueues on `stream` a device-to-device
+ * copy of the first `bytes` bytes of the fixed scratch array that
+ * gbmm_matmul_id_static_scratch uses on the current device, into the
+ * caller's device buffer `dst`: the expert counts (u32[GBMM_GROUPED_MAX_EXPERTS])
+ * first, then the routed-row lists (u32, expert e's list at entry e * m of
+ * that region, m the last call's token count).  Lets a test check the routing
+ * map the last call left there.  GBMM_ERR_INVALID_ARGUMENT when `bytes`
+ * exceeds the array or `dst` is NULL.
+ */
+GBMM_API gbmm_status gbmm_test_static_scratch_copy(void *dst, uint64_t bytes, gbmm_stream stream);
 
 #ifdef __cplusplus
 }

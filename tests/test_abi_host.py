@@ -31,6 +31,19 @@ def lib():
     return gb.load()
 
 
+@pytest.fixture(autouse=True)
+def _no_kernel_may_launch():
+    """Every kernel launch is blocked while a case here runs: on a machine
+    with a GPU, a validation rule that regressed then shows up as
+    GBMM_ERR_KERNEL_UNAVAILABLE instead of a kernel reading the fake
+    addresses below."""
+    gbuild.build()
+    gb.load()
+    gb.gbmm_test_inject_kernel_failure("*")
+    yield
+    gb.gbmm_test_inject_kernel_failure(None)
+
+
 def _declared_symbols():
     with open(os.path.join(ROOT, "include", "gbmm.h")) as f:
         text = f.read()

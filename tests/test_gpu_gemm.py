@@ -215,6 +215,32 @@ def test_tc_gemm_wide_tiles_broadcast_sampled(oracle_mod, dtype, ta, tb, bcast):
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc", idx=np.array(idx, dtype=np.int64))
 
 
+@pytest.mark.parametrize("dtype,ta,tb,k", [("f16", False, True, 512), ("bf16", True, False, 1000)])
+def test_tc_gemm_wide_tiles_every_output(oracle_mod, dtype, ta, tb, k):
+    """The 256 x 256-tile kernel compared on EVERY output.  m = 4000, n = 5000:
+    16 x 20 = 320 tiles with ragged last row and column tiles; on the 152 SMs
+    of a GB300 that is two full rounds of tiles (k >= 512 and at least two
+    rounds take the wide kernel) and a last round of 16 tiles, run as 128-row
+    half units.  k = 512 is eight whole k-blocks; k = 1000 ends on a ragged one
+    and wraps the three-stage operand ring five times."""
+    batch, m, n = 1, 4000, 5000
+    lda = _up8(m if ta else k)
+    ldb = _up8(k if tb else n)
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, lda=lda, ldb=ldb, std=1.0 / np.sqrt(k), seed=k + ta)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("reading", ["b_m_k_n", "b_m_n_k"])
+def test_tc_gemm_page_shape_25_1280_32000(oracle_mod, dtype, reading):
+    """The tract-metal tests' (1, 25, 1280, 32000) matmul on the tensor cores
+    (both readings of the tuple order), B stored [n, k]: every output."""
+    b, m, x, y = 1, 25, 1280, 32000
+    n, k = (y, x) if reading == "b_m_k_n" else (x, y)
+    g = StridedGemm(dtype, b, m, n, k, False, True, std=1.0 / np.sqrt(k), seed=25 + k)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc")
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_tc_gemm_exact_small_integers(oracle_mod, dtype):
     # |v| <= 8 integers, k = 1024: every product and partial sum is an exact

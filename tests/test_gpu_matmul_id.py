@@ -264,6 +264,18 @@ def test_grouped_tc_tail_units(oracle_mod):
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
 
 
+def test_grouped_tc_deep_k_every_output(oracle_mod):
+    """k = 4096 (64 k-blocks: the three-stage weight and activation rings wrap
+    about 21 times per tile), 2048 tokens x top-2 over 4 experts (about 1024
+    routed rows each: 8 row blocks of 128), n = 1536 (three 512-column
+    blocks): 96 whole tiles.  Every output and the map."""
+    m, top_k, E = 2048, 2, 4
+    case = synth.matmul_id_case("deepk", "bf16", m, 1536, 4096, top_k, E, route=1, seed=21)
+    r = Run(case).call()
+    r.check(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+
+
 @pytest.mark.parametrize("k", [40, 104, 136, 200, 264, 328, 448])
 def test_grouped_tc_k_block_orders(oracle_mod, k):
     """1 to 7 k-blocks of 64 (ragged or whole), the short-k end of the
