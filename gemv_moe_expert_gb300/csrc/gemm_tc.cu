@@ -552,7 +552,10 @@ gemm_tc_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     if (row < p.m && col0 < p.n) {
                         if (p.c_vec_ok == 2 && col0 + 32 <= p.n) {
                             // whole 32-byte sectors per store (this epilogue is not
-                            // overlapped with MMAs: its store rate shows directly)
+                            // overlapped with MMAs: its store rate shows directly),
+                            // streaming: C is not read again here, and lines marked
+                            // evict-first leave L2 (written back) while the GEMM still
+                            // runs instead of during the next kernel's reads
 #pragma unroll
                             for (int v = 0; v < 2; ++v) {
                                 uint32_t o[8];
@@ -560,7 +563,7 @@ gemm_tc_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                                 for (int q = 0; q < 8; ++q)
                                     o[q] = pack2<TC>(__uint_as_float(r[16 * v + 2 * q]),
                                                      __uint_as_float(r[16 * v + 2 * q + 1]));
-                                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                                asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
                                                  crow + col0 + 16 * v),
                                              "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
                                              "r"(o[6]), "r"(o[7])
@@ -575,7 +578,7 @@ gemm_tc_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                                 o.y = pack2<TC>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
                                 o.z = pack2<TC>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
                                 o.w = pack2<TC>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                                dst[v] = o;
+                                __stcs(dst + v, o);
                             }
                         } else {
 #pragma unroll

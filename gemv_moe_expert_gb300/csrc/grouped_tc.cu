@@ -44,6 +44,20 @@
 // Tile list: every CTA derives it from expert_counts (written by the map
 // launch before this one): tiles ordered by expert, then row block, then
 // output block.  Every mbarrier wait is bounded; see gemm_tc.cu.
+//
+// Tail units.  An expert's last row block often holds only a few routed rows
+// (on the Zipf prefill workload 69 of 128 experts end on a block of at most
+// 64), yet an M = 128 MMA costs the same for 38 rows as for 128.  A unit
+// whose row block holds r <= 64 routed rows therefore swaps the operands:
+// the weights are the MMA's M side (each 256-row weight stage is two
+// 128-row A tiles) and the routed rows its N side, hi in operand rows 0..r-1
+// and lo in rows 64..63+r of the activation stage, N = 64 + round16(r)
+// (round16(r) without the lo half).  MMAs with N below ~112 cost a fixed ~55
+// cycles, so the unit's 16 MMAs per k-block cost 16 x ~55-64 cycles instead
+// of 16 x 128.  Its four accumulators (one per 128 outputs) sit 128 TMEM
+// columns apart; the epilogue adds columns c and 64 + c of a lane (an output
+// column) and writes routed row c, a warp covering 32 consecutive outputs.
+// The arithmetic is the same bf16 hi + lo products as the other units.
 #include "device_common.cuh"
 
 namespace gbmm {
@@ -51,6 +65,9 @@ namespace gbmm {
 namespace {
 
 constexpr int kBM = 128;
+constexpr int kTailRows = 64;      // row blocks of at most this many routed rows run as tail units
+constexpr int kTailLo = 64;        // operand row of the lo half of routed row 0 in a tail unit
+constexpr uint32_t kTailCols = 128;  // TMEM columns between the accumulators of a tail unit
 constexpr int kBNH = 256;          // one accumulator / one MMA N
 constexpr int kBN = 2 * kBNH;      // tile width
 constexpr int kBK = 64;
@@ -70,11 +87,24 @@ constexpr uint32_t kRingBytes = kWBase + kWStages * kWBytes;
 constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 4;
 constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 8 * kNumBars + 16 + 1024;
 
+static_assert(kTailLo % 8 == 0 && kTailRows <= kTailLo && kTailLo + kTailRows <= kBM,
+              "a tail unit's hi and lo rows share the 128-row x_hi operand, in the same swizzle phase");
+static_assert(4 * kTailCols <= kTmemCols && kTailLo + kTailRows <= static_cast<int>(kTailCols),
+              "four tail accumulators of at most 128 columns fill the tensor memory");
+
 struct GroupedTile {
     int e, mb, nb, rows;
     int n0;      // first output column of the work unit
     int halves;  // 256-column accumulator halves it computes (0: nothing to do)
+    bool tail;   // rows <= kTailRows: routed rows on the MMA's N side
 };
+
+// MMA N of a tail unit with `rows` routed rows: hi rows at 0.., lo rows at kTailLo..
+template <bool kSplit>
+__device__ __forceinline__ uint32_t tail_n(int rows) {
+    const uint32_t r16 = static_cast<uint32_t>(rows + 15) & ~15u;
+    return kSplit ? static_cast<uint32_t>(kTailLo) + r16 : r16;
+}
 
 // expert of tile t: the largest e with prefix[e] <= t (prefix has E+1 entries)
 __device__ __forceinline__ GroupedTile decode_grouped(int t, const uint32_t *prefix, int E, int nblk,
@@ -91,6 +121,7 @@ __device__ __forceinline__ GroupedTile decode_grouped(int t, const uint32_t *pre
     g.nb = local % nblk;
     const int cnt = min(static_cast<int>(counts[lo]), m);
     g.rows = min(kBM, cnt - g.mb * kBM);
+    g.tail = g.rows <= kTailRows;
     return g;
 }
 
@@ -279,6 +310,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
                 const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
                 if (g.halves == 0) continue;
+                // tail unit: weights as A (M = 128), the routed rows as B (N rows)
+                const uint32_t idesc_tail = idesc_f16(1u, kBM, tail_n<kSplit>(g.rows));
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
                     if (!mbar_wait_bounded(xfull_bar(xs), xph, lim, abort_flag)) {
                         ok = false;
@@ -286,7 +319,32 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     }
                     const uint32_t s_hi = s_base + xs * kXStageBytes;
                     const uint32_t s_lo = s_hi + kXBytes;
-                    for (int h = 0; h < g.halves; ++h) {
+                    for (int h = 0; h < g.halves && g.tail; ++h) {
+                        if (kb == 0 && !mbar_wait_bounded(tempty_bar(h), acc_phase[h] ^ 1u, lim, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait_bounded(wfull_bar(ws), wph, lim, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t s_w = s_base + kWBase + ws * kWBytes;
+#pragma unroll
+                        for (int m2 = 0; m2 < 2; ++m2) {
+                            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(2 * h + m2) * kTailCols;
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_w + m2 * (kBM * 128) + kk * 32),
+                                            sdesc_kmajor_sw128(s_hi + kk * 32), idesc_tail, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        umma_commit(wempty_bar(ws));
+                        if (++ws == kWStages) {
+                            ws = 0;
+                            wph ^= 1u;
+                        }
+                    }
+                    for (int h = 0; h < g.halves && !g.tail; ++h) {
                         // accumulator half h drained by the epilogue of the previous unit
                         if (kb == 0 && !mbar_wait_bounded(tempty_bar(h), acc_phase[h] ^ 1u, lim, abort_flag)) {
                             ok = false;
@@ -345,6 +403,39 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 break;
             }
             tc_fence_after();
+            if (g.tail) {
+                // lane = output column n0 + 128 q + 32 quarter + lane; TMEM column
+                // c (hi) + column kTailLo + c (lo) of accumulator q = routed row c
+                const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+                const int64_t row_base = static_cast<int64_t>(g.e) * m + g.mb * kBM;
+                for (int q = 0; q < 2 * g.halves; ++q) {
+                    const int64_t j = static_cast<int64_t>(g.n0) + q * kBM + quarter * 32 + lane;
+                    for (int c0 = 0; c0 < g.rows; c0 += 32) {
+                        uint32_t vh[32], vl[32];
+                        tmem_ld32(t_lane + static_cast<uint32_t>(q) * kTailCols + c0, vh);
+                        if (kSplit) tmem_ld32(t_lane + static_cast<uint32_t>(q) * kTailCols + kTailLo + c0, vl);
+                        tmem_ld_wait();
+                        const uint32_t my_r = c0 + lane < g.rows ? p.routed_rows[row_base + c0 + lane] : 0u;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const uint32_t r = __shfl_sync(0xffffffffu, my_r, c);
+                            if (c0 + c < g.rows && j < p.n) {
+                                const float v = kSplit ? __uint_as_float(vh[c]) + __uint_as_float(vl[c])
+                                                       : __uint_as_float(vh[c]);
+                                __stcs(p.out + static_cast<int64_t>(r) * p.n + j, v);
+                            }
+                        }
+                    }
+                    if (q & 1) {
+                        // both accumulators of this 256-column half are read: hand it back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(q >> 1));
+                    }
+                }
+                acc_phase ^= 1u;
+                continue;
+            }
             const int i = quarter * 32 + lane;
             const bool valid = i < g.rows;
             const int64_t r = valid ? static_cast<int64_t>(p.routed_rows[static_cast<int64_t>(g.e) * m +
@@ -452,6 +543,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 #pragma unroll
                 for (int q = 0; q < kRowsPerProducer; ++q) {
                     const int i = rsub + 32 * q;
+                    // a tail unit keeps its lo rows where the hi rows past its count would go
+                    if (g.tail && i >= g.rows) continue;
                     const float f[8] = {buf[q][0].x, buf[q][0].y, buf[q][0].z, buf[q][0].w,
                                         buf[q][1].x, buf[q][1].y, buf[q][1].z, buf[q][1].w};
                     uint32_t hi[4], lo[4];
@@ -467,8 +560,12 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + off), "r"(hi[0]),
                                  "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
                                  : "memory");
+                    // lo: row kTailLo + i of the same operand in a tail unit (same
+                    // swizzle phase: kTailLo is a multiple of 8), else row i of x_lo
+                    const uint32_t lo_addr = g.tail ? s_hi + off + static_cast<uint32_t>(kTailLo) * 128u
+                                                    : s_hi + kXBytes + off;
                     if (kSplit)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_hi + kXBytes + off),
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(lo_addr),
                                      "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
                                      : "memory");
                 }

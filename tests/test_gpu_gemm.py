@@ -215,14 +215,14 @@ def test_tc_gemm_wide_tiles_broadcast_sampled(oracle_mod, dtype, ta, tb, bcast):
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_tc", idx=np.array(idx, dtype=np.int64))
 
 
-@pytest.mark.parametrize("dtype,ta,tb,k", [("f16", False, True, 512), ("bf16", True, False, 1000)])
+@pytest.mark.parametrize("dtype,ta,tb,k", [("f16", False, True, 512), ("bf16", True, False, 520)])
 def test_tc_gemm_wide_tiles_every_output(oracle_mod, dtype, ta, tb, k):
     """The 256 x 256-tile kernel compared on EVERY output.  m = 4000, n = 5000:
     16 x 20 = 320 tiles with ragged last row and column tiles; on the 152 SMs
     of a GB300 that is two full rounds of tiles (k >= 512 and at least two
     rounds take the wide kernel) and a last round of 16 tiles, run as 128-row
-    half units.  k = 512 is eight whole k-blocks; k = 1000 ends on a ragged one
-    and wraps the three-stage operand ring five times."""
+    half units.  k = 512 is eight whole k-blocks; k = 520 ends on a ragged
+    ninth one (the three-stage operand ring wraps three times)."""
     batch, m, n = 1, 4000, 5000
     lda = _up8(m if ta else k)
     ldb = _up8(k if tb else n)

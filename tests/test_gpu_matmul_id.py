@@ -266,13 +266,46 @@ def test_grouped_tc_tail_units(oracle_mod):
 
 def test_grouped_tc_deep_k_every_output(oracle_mod):
     """k = 4096 (64 k-blocks: the three-stage weight and activation rings wrap
-    about 21 times per tile), 2048 tokens x top-2 over 4 experts (about 1024
-    routed rows each: 8 row blocks of 128), n = 1536 (three 512-column
-    blocks): 96 whole tiles.  Every output and the map."""
-    m, top_k, E = 2048, 2, 4
-    case = synth.matmul_id_case("deepk", "bf16", m, 1536, 4096, top_k, E, route=1, seed=21)
+    about 21 times per tile), 1664 tokens x top-2 over 4 experts (about 832
+    routed rows each: 7 row blocks of 128), n = 1088 (two 512-column blocks
+    and a 64-column one): 84 whole tiles.  Every output and the map."""
+    m, top_k, E = 1664, 2, 4
+    case = synth.matmul_id_case("deepk", "bf16", m, 1088, 4096, top_k, E, route=1, seed=21)
     r = Run(case).call()
     r.check(oracle_mod)
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+
+
+# routed rows per expert: last row blocks of every size around the tail-unit
+# limit (64 rows: such blocks run with the routed rows on the MMA's N side,
+# hi rows 0.., lo rows 64..) and the N = 16 steps, plus experts of several
+# blocks and one with none
+TAIL_COUNTS = [1, 15, 16, 17, 31, 32, 33, 47, 48, 63, 64, 65, 96, 133, 192, 257, 0, 128 + 64]
+
+
+@pytest.mark.parametrize("n,k,precision", [(1536, 264, 0), (2560, 200, 0), (1100, 104, 0), (1536, 264, 1)],
+                         ids=["halves", "whole", "cut-past-n", "single-rounding"])
+def test_grouped_tc_tail_units_every_size(oracle_mod, n, k, precision):
+    """Last row blocks of 1..65 routed rows (top_k 1, one id per token, the
+    tokens shuffled over the experts).  n = 1536: 22 row blocks x 3 column
+    blocks = 66 tiles, at most half the CTAs, so every tile runs as two
+    256-column halves; n = 2560: 110 whole tiles; n = 1100: the second half
+    of each last column block lies past n.  Every output and the map; the
+    single-rounding mode within its own bound."""
+    counts = np.array(TAIL_COUNTS)
+    m, top_k, E = int(counts.sum()), 1, len(counts)
+    rng = np.random.default_rng(5)
+    ids = rng.permutation(np.repeat(np.arange(E), counts)).astype(np.uint32).reshape(m, 1)
+    case = synth.matmul_id_case("tails", "bf16", m, n, k, top_k, E, route=1, ids=ids, seed=k)
+    r = Run(case, precision=precision).call()
+    if precision == 0:
+        r.check(oracle_mod)
+    else:
+        got = r.output()
+        ref, ref_abs = oracle_mod.matmul_id("bf16", m, n, k, top_k, E, case.expert_stride_bytes, 0,
+                                            case.w, case.x, case.ids)
+        assert np.all(np.abs(got - ref.reshape(-1)) <= (2.0 ** -8 + 1e-5) * ref_abs.reshape(-1))
+        r.check_map(oracle_mod)
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
 
 
