@@ -604,7 +604,8 @@ def run_ours(args) -> None:
         quick = argparse.Namespace(steps=5, warmup=2)
         t_side = time.perf_counter()
         for name, fn in (("skinny_gemv", sweep_skinny), ("route_crossover", sweep_crossover),
-                         ("matmul_id_dtypes", sweep_dtypes), ("ffma_gemm", sweep_ffma)):
+                         ("matmul_id_dtypes", sweep_dtypes), ("ffma_gemm", sweep_ffma),
+                         ("c3_cublas_context", cublas_context)):
             side[name] = fn(quick, torch, gb, quick=True)
             torch.cuda.empty_cache()
         side["seconds"] = time.perf_counter() - t_side
@@ -714,16 +715,18 @@ def run_reference(args) -> None:
 # ---------------------------------------------------------------------------
 
 def _time_alone(call, torch, flush, steps, warmup):
-    """Median of `steps` calls, each timed with CUDA events after an L2 flush.
-    A device-side spin (about 0.2 ms) is queued between the flush and the start
-    event so that the host has enqueued the call before the GPU reaches the
-    event: the interval holds the call's device time, not the host's argument
-    marshalling and launch latency."""
+    """Mean of max(steps, 12) calls, each timed with CUDA events after an L2
+    flush.  A device-side spin (about 0.2 ms) is queued between the flush and
+    the start event so that the host has enqueued the call before the GPU
+    reaches the event: the interval holds the call's device time, not the
+    host's argument marshalling and launch latency.  The mean, not the median:
+    on this GPU one event interval reads in steps of about 2.05 us, and the
+    mean of many readings resolves what a median of them rounds away."""
     for _ in range(warmup):
         call()
     torch.cuda.synchronize()
     ts = []
-    for _ in range(steps):
+    for _ in range(max(steps, 12)):
         flush.fill_(1)
         torch.cuda._sleep(400_000)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -732,7 +735,7 @@ def _time_alone(call, torch, flush, steps, warmup):
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1) * 1e3)
-    return statistics.median(ts)
+    return statistics.mean(ts)
 
 
 def _with_clocks(fn):
@@ -955,6 +958,41 @@ def sweep_dtypes(args, torch, gb, quick=False) -> dict:
     return {"sweep": "matmul_id weight dtypes, layouts and multiplicity", "experts": E, "top_k": top_k,
             "k": k, "n": n, "timing": "each call alone after an L2 flush, median of %d" % args.steps,
             "rows": rows, "clocks": clk}
+
+
+def cublas_context(args, torch, gb, quick=False) -> dict:
+    """Context only (never a baseline of ours): cuBLAS through torch.bmm on
+    the batched f16 GEMM workload's shape (4 x 4096^3, B stored [n, k]), timed
+    alone after an L2 flush and back to back, beside this library's call of
+    the same shape timed the same way."""
+    b, m, n, k = 4, 4096, 4096, 4096
+    g = torch.Generator(device="cuda").manual_seed(0)
+    a = (torch.randn(b * m * k, device="cuda", generator=g) / 64).half()
+    bt = (torch.randn(b * n * k, device="cuda", generator=g) / 64).half()
+    c = torch.empty(b * m * n, device="cuda", dtype=torch.float16)
+    a3, b3 = a.view(b, m, k), bt.view(b, n, k)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def ours():
+        gb.check(gb.gbmm_gemm("f16", b, m, n, k, 0, 1, a, 0, k, m * k, bt, 0, k, n * k, c, 0, n, m * n))
+
+    def theirs():
+        torch.bmm(a3, b3.transpose(1, 2))
+
+    flops = 2 * b * m * n * k
+    out = {"shape": "f16 batch 4, 4096^3, B stored [n, k]", "note": "cuBLAS (torch.bmm) as context only"}
+    for name, fn in (("gbmm", ours), ("cublas", theirs)):
+        us = _time_alone(fn, torch, flush, args.steps, args.warmup)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(20):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        b2b = e0.elapsed_time(e1) * 1e3 / 20
+        out[name] = {"us_alone": us, "us_back_to_back": b2b, "tflops_alone": flops / (us * 1e-6) / 1e12,
+                     "tflops_back_to_back": flops / (b2b * 1e-6) / 1e12}
+    return out
 
 
 def run_sweep(args, fn) -> None:

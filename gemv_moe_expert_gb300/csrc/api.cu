@@ -317,13 +317,18 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
         const int64_t tiles_m = (m + bm - 1) / bm;
         const int64_t tiles = tiles_m * tiles_n * batch;
         const bool a_bc = sa == 0 || batch == 1, b_bc = sb == 0 || batch == 1;
+        // the wide tiles of two K-contiguous operands run on CTA pairs, each
+        // CTA loading 128 rows of A and 128 rows of B
+        const bool pair = wide && !ta && tb;
+        const uint32_t abox = static_cast<uint32_t>(pair ? gemm_tc_block_m() : bm);
+        const uint32_t bbox = static_cast<uint32_t>(pair ? gemm_tc_block_m() : bn);
         // A: [m, k] K-contiguous, or stored [k, m] when transposed; B: [n, k]
         // K-contiguous when transposed, else stored [k, n]
         CUtensorMap map_a, map_b;
         const bool maps_ok =
             (ta ? encode_operand(&map_a, dt, pa, m, k, batch, lda, sa, a_bc, static_cast<uint32_t>(bk))
-                : encode_operand(&map_a, dt, pa, k, m, batch, lda, sa, a_bc, static_cast<uint32_t>(bm))) &&
-            (tb ? encode_operand(&map_b, dt, pb, k, n, batch, ldb, sb, b_bc, static_cast<uint32_t>(bn))
+                : encode_operand(&map_a, dt, pa, k, m, batch, lda, sa, a_bc, abox)) &&
+            (tb ? encode_operand(&map_b, dt, pb, k, n, batch, ldb, sb, b_bc, bbox)
                 : encode_operand(&map_b, dt, pb, n, k, batch, ldb, sb, b_bc, static_cast<uint32_t>(bk)));
         if (tiles < (1LL << 31) && maps_ok) {
             if (!resolve("gbmm_gemm_tc")) return GBMM_ERR_KERNEL_UNAVAILABLE;
@@ -349,8 +354,9 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
             p.num_tiles = static_cast<int32_t>(tiles);
             p.err = err;
             p.wait_limit_ns = kWaitLimitNs;
-            return after_launch(wide ? launch_gemm_tc_wide(dt, map_a, map_b, p, device_sm_count(), stream)
-                                     : launch_gemm_tc(dt, map_a, map_b, p, device_sm_count(), stream),
+            return after_launch(pair   ? launch_gemm_tc_pair(dt, map_a, map_b, p, device_sm_count(), stream)
+                                : wide ? launch_gemm_tc_wide(dt, map_a, map_b, p, device_sm_count(), stream)
+                                       : launch_gemm_tc(dt, map_a, map_b, p, device_sm_count(), stream),
                                 "gbmm_gemm_tc", stream);
         }
     }

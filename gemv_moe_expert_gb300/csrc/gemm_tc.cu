@@ -604,6 +604,308 @@ gemm_tc_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair tiles (A and B both K-contiguous): 256 x 256 outputs per pair of
+// CTAs, computed by tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).
+// Each CTA of the pair holds 128 rows of the A tile and 128 rows of the B
+// tile per k-block (16 KB + 16 KB: half the operand bytes per SM of the
+// 256 x 256 single-CTA tile for the same MMA work per SM) and its tensor
+// memory holds its 128 rows of the accumulator.  A 128 x 256 accumulator
+// per CTA leaves room for a second one, so the epilogue of a tile overlaps
+// the MMAs of the next, and the smaller stages allow a six-deep ring.
+//   warp 0      TMA (both CTAs): this CTA's A and B rows of each k-block,
+//               completion counted on the even CTA's full barrier
+//               (cp.async.bulk.tensor .cta_group::2)
+//   warp 1      allocates 512 TMEM columns in both CTAs (one warp of each
+//               executes the pair allocation); in the even CTA, one thread
+//               issues the pair MMAs and commits them to both CTAs' barriers
+//   warps 2..5  epilogue (both CTAs): their TMEM lane quarter of the tile's
+//               accumulator, rounded and stored; the accumulator is handed
+//               back to the even CTA's MMA issuer (8 arrivals per use)
+// Tiles are visited by clusters in the grouped raster of the other kernels;
+// when the last round of tiles would leave at least half of the pairs idle,
+// its tiles run as two 256 x 128 half units each (N = 128 MMAs, each CTA
+// using the first 64 of the 128 B rows it loads).  Every wait is bounded; a timeout raises both CTAs' abort flags and the
+// device error word; both CTAs meet at a cluster barrier before the tensor
+// memory is released.
+// ---------------------------------------------------------------------------
+
+constexpr int kPStages = 6;
+constexpr uint32_t kPABytes = kBM * kBK * 2;     // this CTA's 128 A rows of a k-block
+constexpr uint32_t kPBBytes = kBM * kBK * 2;     // this CTA's 128 B rows of a k-block
+constexpr uint32_t kPStageBytes = kPABytes + kPBBytes;
+constexpr uint32_t kPSmemBytes = kPStages * kPStageBytes + 256 + 1024;
+static_assert(kPStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+template <typename TC, uint32_t kFmt>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                    const GemmTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t s0 = raw_addr + pad;  // stage s: A at s0 + s * kPStageBytes, B kPABytes after it
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPStages * kPStageBytes);
+    // barrier slots: full[kPStages] (used in the even CTA: both CTAs' copies),
+    // empty[kPStages], tfull[2], tempty[2] (used in the even CTA), drain
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kPStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kPStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kPStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kPStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kPStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
+    const bool leader = rank == 0;
+    const uint64_t lim = p.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(full_bar(s), 1);   // the even CTA's producer arrive + both CTAs' bytes
+            mbar_init(empty_bar(s), 1);  // the pair MMAs' commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 8);  // four epilogue warps in each CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers exist before any copy, commit or arrival can reach them
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kblocks = (p.k + kBK - 1) / kBK;
+    const int cl = static_cast<int>(blockIdx.x) >> 1;
+    const int ncl = static_cast<int>(gridDim.x) >> 1;
+    // the last round of tiles, when it would leave at least half of the pairs
+    // idle, runs as 256 x 128 half units (N = 128 pair MMAs)
+    const int tail = gemm_tail_tiles(p.num_tiles, ncl);
+    const int split_from = p.num_tiles - tail;
+    const int num_units = split_from + 2 * tail;
+    // a timeout stops both CTAs of the pair
+    const uint32_t peer_abort = mapa_shared(smem_addr(const_cast<int *>(abort_flag)), rank ^ 1u);
+    auto raise_abort = [&]() {
+        *abort_flag = 1;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+        report_device_error(p.err, kKidGemmTc);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = cl; u < num_units && ok; u += ncl) {
+                const TileCoord tc = decode_unit(u, split_from, p);
+                if (tc.halves == 0) continue;
+                const int abat = p.a_bcast ? 0 : tc.bat, bbat = p.b_bcast ? 0 : tc.bat;
+                const int arow = tc.mb * 2 * kBM + static_cast<int>(rank) * kBM;
+                // a half unit needs 64 B rows per CTA: the first half of the box
+                const int brow = tc.halves == 2 ? tc.nb * kBN + static_cast<int>(rank) * kBM
+                                                : tc.nb * kBN + tc.h * (kBN / 2) + static_cast<int>(rank) * (kBM / 2);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, lim, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPStageBytes);
+                    const uint32_t sa = s0 + stage * kPStageBytes;
+                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                    tma_load_3d_pair(sa, &map_a, fb, kb * kBK, arow, abat);
+                    tma_load_3d_pair(sa + kPABytes, &map_b, fb, kb * kBK, brow, bbat);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                raise_abort();
+                // copies still in flight land within microseconds; give them 200 us
+                const uint64_t t0 = global_ns();
+                while (global_ns() - t0 < 200000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- pair MMA issuer (even CTA) ----------------
+            constexpr uint32_t kIdesc = idesc_f16(kFmt, 2 * kBM, kBN);
+            constexpr uint32_t kIdescHalf = idesc_f16(kFmt, 2 * kBM, kBN / 2);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_phase[2] = {0u, 0u};
+            bool ok = true;
+            int local = 0;
+            for (int u = cl; u < num_units && ok; u += ncl) {
+                const TileCoord tc = decode_unit(u, split_from, p);
+                if (tc.halves == 0) continue;
+                const uint32_t idesc = tc.halves == 2 ? kIdesc : kIdescHalf;
+                const int a = local++ & 1;
+                // both CTAs' epilogues have read this accumulator's previous tile
+                if (!mbar_wait_bounded_cluster(tempty_bar(a), acc_phase[a] ^ 1u, lim, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * kBN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded_cluster(full_bar(stage), phase, lim, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = s0 + stage * kPStageBytes, sb = sa + kPABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_f16_ss_pair(d_tmem, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
+                                         idesc, (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(empty_bar(stage), 0x3);  // the stage is free in both CTAs
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(tfull_bar(a), 0x3);
+                acc_phase[a] ^= 1u;
+            }
+            if (!ok) raise_abort();
+            umma_commit_pair_mc(drain_bar, 0x1);
+            mbar_wait_bounded(drain_bar, 0, lim, nullptr);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        uint32_t tphase[2] = {0u, 0u};
+        int local = 0;
+        for (int u = cl; u < num_units; u += ncl) {
+            const TileCoord tc = decode_unit(u, split_from, p);
+            if (tc.halves == 0) continue;
+            const int a = local++ & 1;
+            int ready = 0;
+            if (lane == 0) ready = mbar_wait_bounded_cluster(tfull_bar(a), tphase[a], lim, abort_flag);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) {
+                if (lane == 0) raise_abort();
+                break;
+            }
+            __syncwarp();
+            tc_fence_after();
+            const int64_t row = static_cast<int64_t>(tc.mb) * 2 * kBM + static_cast<int64_t>(rank) * kBM +
+                                quarter * 32 + lane;
+            TC *crow = static_cast<TC *>(p.c) + static_cast<int64_t>(tc.bat) * p.sc + row * p.ldc;
+            const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                    static_cast<uint32_t>(a * kBN);
+            const int nchunks = tc.halves == 2 ? kBN / 32 : kBN / 64;
+            const int64_t cbase = static_cast<int64_t>(tc.nb) * kBN + (tc.halves == 2 ? 0 : tc.h * (kBN / 2));
+#pragma unroll 1
+            for (int chunk = 0; chunk < nchunks; ++chunk) {
+                uint32_t r[32];
+                tmem_ld32(t_addr + chunk * 32, r);
+                tmem_ld_wait();
+                const int64_t col0 = cbase + chunk * 32;
+                if (row < p.m && col0 < p.n) {
+                    if (p.c_vec_ok == 2 && col0 + 32 <= p.n) {
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                o[q] = pack2<TC>(__uint_as_float(r[16 * v + 2 * q]),
+                                                 __uint_as_float(r[16 * v + 2 * q + 1]));
+                            asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                                             crow + col0 + 16 * v),
+                                         "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]),
+                                         "r"(o[7])
+                                         : "memory");
+                        }
+                    } else if (p.c_vec_ok && col0 + 32 <= p.n) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack2<TC>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                            o.y = pack2<TC>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                            o.z = pack2<TC>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                            o.w = pack2<TC>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            __stcs(dst + v, o);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (col0 + c < p.n) crow[col0 + c] = Elem<TC>::from_f(__uint_as_float(r[c]));
+                    }
+                }
+            }
+            // this CTA's rows of the accumulator are read: hand it back to the even CTA's issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(a), 0));
+            tphase[a] ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // every pair MMA has completed (the even CTA waited for its drain) and
+    // both CTAs' epilogues are done before either CTA releases the columns
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <typename TC, uint32_t kFmt>
+cudaError_t tc_pair_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
+                      cudaStream_t s) {
+    static unsigned long long attr_set = 0;  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel<TC, kFmt>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set |= bit;
+    }
+    const int pairs = num_sms / 2;
+    const int clusters = 2 * p.num_tiles <= pairs ? 2 * p.num_tiles : (p.num_tiles < pairs ? p.num_tiles : pairs);
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<TC, kFmt>, ma, mb, p);
+}
+
 template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
 cudaError_t tc_wide_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
                       cudaStream_t s) {
@@ -671,6 +973,16 @@ cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &
     switch (dt) {
     case kF16: return tc_major<__half, 0>(map_a, map_b, p, num_sms, s);
     case kBF16: return tc_major<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemm_tc_pair(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                const GemmTcParams &p, int num_sms, cudaStream_t s) {
+    if (p.a_mn || p.b_mn) return cudaErrorInvalidValue;
+    switch (dt) {
+    case kF16: return tc_pair_t<__half, 0>(map_a, map_b, p, num_sms, s);
+    case kBF16: return tc_pair_t<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

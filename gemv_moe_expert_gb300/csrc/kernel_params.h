@@ -131,6 +131,10 @@ cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &
 // box is gemm_tc_wide_block_m() rows when A is K-contiguous
 cudaError_t launch_gemm_tc_wide(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                 const GemmTcParams &p, int num_sms, cudaStream_t s);
+// the same 256 x 256 tiles over CTA pairs (tcgen05 cta_group::2), A and B
+// K-contiguous only; both tensor maps with gemm_tc_block_m()-row boxes
+cudaError_t launch_gemm_tc_pair(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                const GemmTcParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s);
