@@ -152,6 +152,26 @@ bool encode_operand(CUtensorMap *map, int dt, const void *base, int64_t inner, i
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map of a column-dot GEMV's matrix: (outputs, k, batch), outputs
+// contiguous, boxes of `box_cols` outputs x `box_rows` k rows, no swizzle.
+bool encode_coldot(CUtensorMap *map, int dt, const void *base, int64_t rows, int64_t k, int64_t batch,
+                   int64_t ks, int64_t bs, uint32_t box_cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const int64_t size = dtype_size(dt);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ks * size),
+                             static_cast<cuuint64_t>(batch > 1 ? bs * size : ks * size * k)};
+    cuuint32_t box[3] = {box_cols, box_rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapDataType ty = dt == kF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dt == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(map, ty, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, int64_t n,
                       int64_t k, int ta_i, int tb_i, const void *a, int64_t a_off, int64_t lda,
                       int64_t sa, const void *b, int64_t b_off, int64_t ldb, int64_t sb, void *c,
@@ -298,6 +318,18 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
         }
         g.vec_ok = g.mat_rs == 1 && a16(g.mat) && s16(g.mat_ks) && s16(g.mat_bs);
         if (!resolve("gbmm_gemv_coldot")) return GBMM_ERR_KERNEL_UNAVAILABLE;
+        // aligned matrices (and no broadcast matrix across a batch) stream by TMA
+        if (g.vec_ok && (g.batch == 1 || g.mat_bs != 0) && g.rows < (1LL << 31) && g.k < (1LL << 31) &&
+            g.batch < (1LL << 31)) {
+            g.err = device_error_word();
+            g.wait_limit_ns = kWaitLimitNs;
+            CUtensorMap map_m;
+            if (g.err != nullptr &&
+                encode_coldot(&map_m, dt, g.mat, g.rows, g.k, g.batch, g.mat_ks, g.mat_bs,
+                              static_cast<uint32_t>(gemv_coldot_stream_box_cols(dt)),
+                              static_cast<uint32_t>(gemv_coldot_stream_box_rows())))
+                return after_launch(launch_gemv_coldot_stream(dt, map_m, g, stream), "gbmm_gemv_coldot", stream);
+        }
         return after_launch(launch_gemv_coldot(dt, g, stream), "gbmm_gemv_coldot", stream);
     }
 

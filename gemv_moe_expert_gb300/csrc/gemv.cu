@@ -206,6 +206,167 @@ gemv_coldot_kernel(GemvParams p, int ksplit) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// coldot, staged: the same column-dot GEMV with the matrix streamed by TMA.
+// The register-fed kernel above keeps four 16-byte loads in flight per
+// thread (~37 KB per SM), far fewer bytes than HBM's latency needs, and its
+// long-scoreboard stalls set its pace.  Here a producer warp copies boxes of
+// 512 bytes of outputs x 64 k rows (32 KB) into a two-stage shared-memory
+// ring (three CTAs per SM, so the decode shape's 43 tiles x 8-way k split run
+// in one wave), so the bytes in flight no longer depend on registers; 8 consumer
+// warps reduce each stage (a thread owns 16 bytes of outputs, warp w rows
+// w, w + 8, ... of the stage), then the warps' partial sums are added in
+// shared memory and, with a k split, across the cluster through distributed
+// shared memory in rank order.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+
+constexpr int kCsWarps = 8;                 // consumer warps
+constexpr int kCsThreads = (kCsWarps + 1) * 32;
+constexpr int kCsRows = 64;                 // k rows per stage
+constexpr uint32_t kCsRowBytes = 512;       // one 16-byte vector per consumer lane
+constexpr int kCsStages = 2;
+constexpr uint32_t kCsStageBytes = kCsRows * kCsRowBytes;
+constexpr uint32_t kCsSmem = kCsStages * kCsStageBytes + 2 * kCsStages * 8 + 16 + 1024;
+static_assert(kCsWarps * kCsRowBytes / 2 * 4 <= kCsStages * kCsStageBytes,
+              "the warps' partial sums fit in the drained ring");
+
+template <typename T>
+__global__ void __launch_bounds__(kCsThreads, 3)
+gemv_coldot_stream_kernel(const __grid_constant__ CUtensorMap map, const GemvParams p, int ksplit) {
+    constexpr int V = Elem<T>::kVec;
+    constexpr int TW = kCsRowBytes / sizeof(T);  // outputs per tile
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t s0 = raw + pad;
+    const uint32_t bar0 = s0 + kCsStages * kCsStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kCsStages + s); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kCsStages * kCsStageBytes + 2 * kCsStages * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t tile = blockIdx.x / ksplit;
+    const int rank = static_cast<int>(blockIdx.x % ksplit);  // == rank in the cluster (cluster dims = ksplit)
+    const int64_t kbt = (p.k + kCsRows - 1) / kCsRows;
+    const int64_t kb0 = kbt * rank / ksplit, kb1 = kbt * (rank + 1) / ksplit;
+    const uint64_t lim = p.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kCsStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kCsWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kCsWarps && lane == 0) tma_prefetch_desc(&map);
+    __syncthreads();
+
+    float acc[V];
+    for (int64_t bat = blockIdx.y; bat < p.batch; bat += gridDim.y) {
+        // every stage of the previous batch item was consumed before this one's fills
+        const int64_t it0 = (bat - blockIdx.y) / gridDim.y * (kb1 - kb0);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        if (warp == kCsWarps) {
+            if (lane == 0) {
+                // ---------------- producer ----------------
+                int64_t it = it0;
+                bool ok = true;
+                for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = static_cast<int>(it % kCsStages);
+                    const uint32_t use = static_cast<uint32_t>(it / kCsStages);
+                    if (use > 0 && !mbar_wait_bounded(empty_bar(s), (use - 1u) & 1u, lim, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), kCsStageBytes);
+                    tma_load_3d(s0 + s * kCsStageBytes, &map, full_bar(s), static_cast<int32_t>(tile * TW),
+                                static_cast<int32_t>(kb * kCsRows), static_cast<int32_t>(bat));
+                }
+                if (!ok) {
+                    *abort_flag = 1;
+                    report_device_error(p.err, kKidGemvColdotStream);
+                    // this thread's copies still in flight: its last kCsStages fills at most
+                    for (int64_t j = it - 1; j >= it0 && j >= it - kCsStages; --j)
+                        mbar_wait_bounded(full_bar(static_cast<int>(j % kCsStages)),
+                                          static_cast<uint32_t>(j / kCsStages) & 1u, lim, nullptr);
+                }
+            }
+        } else {
+            // ---------------- consumers ----------------
+            const T *vec = static_cast<const T *>(p.vec) + bat * p.vec_bs;
+            int64_t it = it0;
+            for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = static_cast<int>(it % kCsStages);
+                int ready = 0;
+                if (lane == 0)
+                    ready = mbar_wait_bounded(full_bar(s), static_cast<uint32_t>(it / kCsStages) & 1u, lim, abort_flag);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (!ready) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_device_error(p.err, kKidGemvColdotStream);
+                    }
+                    break;
+                }
+                const uint4 *st = reinterpret_cast<const uint4 *>(smem + s * kCsStageBytes);
+#pragma unroll
+                for (int r = warp; r < kCsRows; r += kCsWarps) {
+                    const int64_t x = kb * kCsRows + r;
+                    // rows past k were zero-filled by the copy; their vector entry is not read
+                    const float v = x < p.k ? Elem<T>::to_f(vec[x * p.vec_ks]) : 0.f;
+                    float wf[V];
+                    unpack16<T>(st[r * (kCsRowBytes / 16) + lane], wf);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] = fmaf(wf[i], v, acc[i]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(s));
+            }
+        }
+        // every stage of this batch item is consumed (or the CTA aborted): the
+        // ring is free for the partial sums of the warps
+        __syncthreads();
+        float *red = reinterpret_cast<float *>(smem);  // [kCsWarps][TW]
+        if (warp < kCsWarps) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) red[warp * TW + lane * V + i] = acc[i];
+        }
+        __syncthreads();
+        float *part = red + kCsWarps * TW;  // [TW]: this CTA's sums
+        for (int c = threadIdx.x; c < TW; c += blockDim.x) {
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCsWarps; ++w) sum += red[w * TW + c];
+            part[c] = sum;
+        }
+        T *out = static_cast<T *>(p.out) + bat * p.out_bs;
+        if (ksplit > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();  // every CTA's partial sums are visible cluster-wide
+            if (rank == 0) {
+                for (int c = threadIdx.x; c < TW; c += blockDim.x) {
+                    float sum = part[c];
+                    for (int q = 1; q < ksplit; ++q) sum += cluster.map_shared_rank(part, q)[c];
+                    const int64_t o = tile * TW + c;
+                    if (o < p.rows) out[o * p.out_os] = Elem<T>::from_f(sum);
+                }
+            }
+            cluster.sync();  // keep the other CTAs' shared memory alive until read
+        } else {
+            __syncthreads();
+            for (int c = threadIdx.x; c < TW; c += blockDim.x) {
+                const int64_t o = tile * TW + c;
+                if (o < p.rows) out[o * p.out_os] = Elem<T>::from_f(part[c]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
 template <typename T>
 __global__ void fill_zero_kernel(T *c, int64_t batch, int64_t m, int64_t n, int64_t ldc, int64_t sc) {
     const int64_t total = batch * m * n;
@@ -276,6 +437,41 @@ cudaError_t coldot_t(const GemvParams &p, cudaStream_t s) {
 }
 
 template <typename T>
+cudaError_t coldot_stream_t(const CUtensorMap &map, const GemvParams &p, cudaStream_t s) {
+    constexpr int TW = kCsRowBytes / sizeof(T);
+    const int64_t tiles = (p.rows + TW - 1) / TW;
+    const int64_t bgrid = p.batch < 65535 ? p.batch : 65535;
+    const int64_t kbt = (p.k + kCsRows - 1) / kCsRows;
+    // split k over a cluster (at most 8) until the grid holds two CTAs per SM,
+    // keeping at least four k-blocks per CTA
+    int ksplit = 1;
+    while (ksplit < 8 && tiles * bgrid * ksplit < 2LL * num_sms() && kbt >= 4LL * ksplit * 2) ksplit *= 2;
+    static unsigned long long attr_set = 0;  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_coldot_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kCsSmem);
+        if (e != cudaSuccess) return e;
+        attr_set |= bit;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * ksplit), static_cast<unsigned>(bgrid), 1);
+    cfg.blockDim = dim3(kCsThreads, 1, 1);
+    cfg.dynamicSmemBytes = kCsSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_coldot_stream_kernel<T>, map, p, ksplit);
+}
+
+template <typename T>
 cudaError_t fill_t(void *c, int64_t batch, int64_t m, int64_t n, int64_t ldc, int64_t sc,
                    cudaStream_t s) {
     const int64_t total = batch * m * n;
@@ -307,6 +503,18 @@ cudaError_t launch_gemv_coldot(int dt, const GemvParams &p, cudaStream_t s) {
     default: return cudaErrorInvalidValue;
     }
 }
+
+cudaError_t launch_gemv_coldot_stream(int dt, const CUtensorMap &map, const GemvParams &p, cudaStream_t s) {
+    switch (dt) {
+    case kF32: return coldot_stream_t<float>(map, p, s);
+    case kF16: return coldot_stream_t<__half>(map, p, s);
+    case kBF16: return coldot_stream_t<__nv_bfloat16>(map, p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemv_coldot_stream_box_cols(int dt) { return static_cast<int>(kCsRowBytes) / (dt == kF32 ? 4 : 2); }
+int gemv_coldot_stream_box_rows() { return kCsRows; }
 
 cudaError_t launch_fill_zero(int dt, void *c, int64_t batch, int64_t m, int64_t n, int64_t ldc,
                              int64_t sc, cudaStream_t s) {

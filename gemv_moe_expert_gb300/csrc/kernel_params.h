@@ -25,6 +25,7 @@ enum KernelId : uint32_t {
     kKidGemvStream = 4,
     kKidGemvTc = 5,
     kKidDirectTc = 6,
+    kKidGemvColdotStream = 7,
 };
 
 // default limit of a bounded device wait (1 s)
@@ -114,6 +115,12 @@ cudaError_t launch_gemv_coldot(int dt, const GemvParams &p, cudaStream_t s);
 // staged-stream GEMV (stream.cu) and the shapes it takes
 bool gemv_stream_eligible(int dt, const GemvParams &p);
 cudaError_t launch_gemv_stream(int dt, const GemvParams &p, int num_sms, cudaStream_t s);
+// column-dot GEMV fed by TMA (gemv.cu): `map` is a 3-D tensor map over
+// (outputs, k, batch) of the matrix with gemv_coldot_stream_box_cols() x
+// gemv_coldot_stream_box_rows() boxes, no swizzle
+cudaError_t launch_gemv_coldot_stream(int dt, const CUtensorMap &map, const GemvParams &p, cudaStream_t s);
+int gemv_coldot_stream_box_cols(int dt);
+int gemv_coldot_stream_box_rows();
 // skinny decode GEMV on the tensor cores (gemv_tc.cu): W boxes of
 // gemv_tc_block_rows() rows, x boxes of gemv_tc_max_tokens() rows, both
 // gemv_tc_block_k() wide

@@ -322,6 +322,26 @@ def test_gemv_parity(oracle_mod, dtype, case, entry):
     assert ratio <= 1.0
 
 
+# the column-dot orientation with an aligned matrix: staged through shared
+# memory by TMA (boxes of 512 bytes of outputs x 64 k rows)
+COLDOT_STREAM_CASES = [
+    # (batch, m, n, k, ta, tb)
+    (1, 1, 704, 1031, False, False),    # x times B stored [k, n]: ragged output tile and k-block
+    (3, 1, 520, 777, False, False),     # batched, batch strides, ragged
+    (2, 776, 1, 999, True, True),       # n == 1 with A stored [k, m]
+    (1, 1, 64, 65536, False, False),    # few outputs, long k: k split over a cluster
+    (1, 1, 11008, 4096, False, False),  # the decode shape, every output
+]
+
+
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+@pytest.mark.parametrize("case", COLDOT_STREAM_CASES, ids=[str(c) for c in COLDOT_STREAM_CASES])
+def test_gemv_coldot_stream_parity(oracle_mod, dtype, case):
+    batch, m, n, k, ta, tb = case
+    g = StridedGemm(dtype, batch, m, n, k, ta, tb, std=1.0, seed=k + n)
+    run_case(oracle_mod, g, fn=gb.gbmm_gemv, expect_kernel="gbmm_gemv_coldot")
+
+
 def test_gemv_decode_workload_c2(oracle_mod):
     """Decode GEMV f16: x [1,4096] ~N(0,1), W [11008,4096] ~N(0,0.02) (tb): all outputs."""
     w = synth.workload("c2_f16_gemv")
