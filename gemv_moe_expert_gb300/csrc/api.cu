@@ -339,9 +339,8 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
                            batch < (1LL << 31);
     if (tc_layout) {
         const int bn = gemm_tc_block_n(), bk = gemm_tc_block_k();
-        // 256-row tiles halve the operand bytes per MMA against 128-row tiles
-        // but keep no second accumulator for the epilogue to overlap with:
-        // taken for long k and at least two rounds of tiles over the SMs
+        // 256 x 256 tiles on CTA pairs: taken for long k and at least two
+        // rounds of tiles over the SMs
         const int wbm = gemm_tc_wide_block_m();
         const int64_t tiles_n = (n + bn - 1) / bn;
         const bool wide = k >= 512 && ((m + wbm - 1) / wbm) * tiles_n * batch >= 2LL * device_sm_count();
@@ -349,9 +348,9 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
         const int64_t tiles_m = (m + bm - 1) / bm;
         const int64_t tiles = tiles_m * tiles_n * batch;
         const bool a_bc = sa == 0 || batch == 1, b_bc = sb == 0 || batch == 1;
-        // the wide tiles of two K-contiguous operands run on CTA pairs, each
-        // CTA loading 128 rows of A and 128 rows of B
-        const bool pair = wide && !ta && tb;
+        // the wide tiles run on CTA pairs, each CTA loading 128 rows (or
+        // columns) of A and of B
+        const bool pair = wide;
         const uint32_t abox = static_cast<uint32_t>(pair ? gemm_tc_block_m() : bm);
         const uint32_t bbox = static_cast<uint32_t>(pair ? gemm_tc_block_m() : bn);
         // A: [m, k] K-contiguous, or stored [k, m] when transposed; B: [n, k]
@@ -386,9 +385,8 @@ gbmm_status gemm_impl(bool gemv_only, gbmm_dtype dt, int64_t batch, int64_t m, i
             p.num_tiles = static_cast<int32_t>(tiles);
             p.err = err;
             p.wait_limit_ns = kWaitLimitNs;
-            return after_launch(pair   ? launch_gemm_tc_pair(dt, map_a, map_b, p, device_sm_count(), stream)
-                                : wide ? launch_gemm_tc_wide(dt, map_a, map_b, p, device_sm_count(), stream)
-                                       : launch_gemm_tc(dt, map_a, map_b, p, device_sm_count(), stream),
+            return after_launch(pair ? launch_gemm_tc_pair(dt, map_a, map_b, p, device_sm_count(), stream)
+                                     : launch_gemm_tc(dt, map_a, map_b, p, device_sm_count(), stream),
                                 "gbmm_gemm_tc", stream);
         }
     }

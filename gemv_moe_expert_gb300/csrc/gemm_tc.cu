@@ -9,9 +9,9 @@
 // `dispatch_metal_mlx_gemm` (B stored [n, k] when transposed; batch strides
 // per operand) and rlx-metal 0.2.14, src/mps_blas.rs (transposeRight).
 //
-// Two kernels: gemm_tc_wide_kernel (256 x 256 tiles, see its section below)
-// for long-k problems with at least two rounds of such tiles, and
-// gemm_tc_kernel (128 x 256 tiles) for the rest; the host picks one.
+// Two kernels: gemm_tc_pair_kernel (256 x 256 tiles on CTA pairs, see its
+// section below) for long-k problems with at least two rounds of such tiles,
+// and gemm_tc_kernel (128 x 256 tiles) for the rest; the host picks one.
 //
 // Design of gemm_tc_kernel (one persistent CTA per SM, 6 warps, warp-specialised):
 //   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles, 128-byte
@@ -332,281 +332,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
 }
 
-// ---------------------------------------------------------------------------
-// Wide tiles: 256 x 256 outputs per tile as two 128-row sub-tiles that share
-// the B tile.  Per 64-wide k-block a CTA takes in 64 KB (A 32 KB + B 32 KB)
-// for eight MMAs, two thirds of the 48 KB per four MMAs of the 128 x 256 tile,
-// which is what limits that tile on long-k problems (its MMA issuer waits a
-// quarter of the time for operands).  The two 128 x 256 f32 accumulators fill
-// the tensor memory, so the epilogue hands each one back as soon as it is
-// stored, and the next tile's first MMAs wait for it.  Three 64 KB stages.
-// When the last round of tiles would leave at least half of the CTAs idle,
-// each of its tiles runs as two 128-row half units.
-// ---------------------------------------------------------------------------
-
-constexpr int kWBM = 256;
-constexpr int kWStages = 3;
-constexpr uint32_t kWABytes = kWBM * kBK * 2;
-constexpr uint32_t kWStageBytes = kWABytes + kBBytes;
-constexpr uint32_t kWSmemBytes = kWStages * kWStageBytes + 256 + 1024;
-
-__device__ __forceinline__ TileCoord decode_unit_wide(int u, int split_from, const GemmTcParams &p) {
-    if (u < split_from) return decode_tile(u, p);
-    TileCoord t = decode_tile(split_from + (u - split_from) / 2, p);
-    t.h = (u - split_from) & 1;
-    t.halves = static_cast<int64_t>(t.mb) * kWBM + t.h * kBM < p.m ? 1 : 0;
-    return t;
-}
-
-template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                    const GemmTcParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
-    uint8_t *smem = smem_raw + pad;
-    const uint32_t s0 = raw_addr + pad;  // stage s: A at s0 + s * kWStageBytes, B kWABytes after it
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWStages * kWStageBytes);
-    // barrier slots: full[kWStages], empty[kWStages], tfull, tempty[2], drain
-    const uint32_t bar0 = smem_addr(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kWStages + s); };
-    const uint32_t tfull_bar = bar0 + 8u * (2 * kWStages);
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kWStages + 1 + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kWStages + 3);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kWStages + 4);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kWStages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        mbar_init(tfull_bar, 1);
-        mbar_init(tempty_bar(0), 4);
-        mbar_init(tempty_bar(1), 4);
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_a);
-        tma_prefetch_desc(&map_b);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-    const int kblocks = (p.k + kBK - 1) / kBK;
-    const int tail = gemm_tail_tiles(p.num_tiles, static_cast<int>(gridDim.x));
-    const int split_from = p.num_tiles - tail;
-    const int num_units = split_from + 2 * tail;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-                const TileCoord tc = decode_unit_wide(u, split_from, p);
-                if (tc.halves == 0) continue;
-                const int abat = p.a_bcast ? 0 : tc.bat, bbat = p.b_bcast ? 0 : tc.bat;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sa = s0 + stage * kWStageBytes, sb = sa + kWABytes;
-                    mbar_arrive_expect_tx(full_bar(stage), kWStageBytes);
-                    if (kAMN) {
-#pragma unroll
-                        for (int j = 0; j < kWBM / 64; ++j)
-                            tma_load_3d(sa + j * kMNBox, &map_a, full_bar(stage), tc.mb * kWBM + j * 64, kb * kBK,
-                                        abat);
-                    } else {
-                        tma_load_3d(sa, &map_a, full_bar(stage), kb * kBK, tc.mb * kWBM, abat);
-                    }
-                    if (kBMN) {
-#pragma unroll
-                        for (int j = 0; j < kBN / 64; ++j)
-                            tma_load_3d(sb + j * kMNBox, &map_b, full_bar(stage), tc.nb * kBN + j * 64, kb * kBK,
-                                        bbat);
-                    } else {
-                        tma_load_3d(sb, &map_b, full_bar(stage), kb * kBK, tc.nb * kBN, bbat);
-                    }
-                    ++issued;
-                    if (++stage == kWStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                report_device_error(p.err, kKidGemmTc);
-                for (int s = 0; s < kWStages; ++s) {
-                    const uint32_t n_s = issued / kWStages + (static_cast<uint32_t>(s) < issued % kWStages ? 1u : 0u);
-                    if (n_s > 0) mbar_wait_bounded(full_bar(s), (n_s - 1u) & 1u, p.wait_limit_ns, nullptr);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t kIdesc = idesc_f16(kFmt, kBM, kBN, kAMN ? 1u : 0u, kBMN ? 1u : 0u);
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t acc_phase[2] = {0u, 0u};
-            bool ok = true;
-            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-                const TileCoord tc = decode_unit_wide(u, split_from, p);
-                if (tc.halves == 0) continue;
-                for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = s0 + stage * kWStageBytes, sb = sa + kWABytes;
-                    for (int a = 0; a < tc.halves; ++a) {
-                        // accumulator a holds rows of sub-tile `sub` (a half unit uses accumulator 0)
-                        const int sub = tc.halves == 2 ? a : tc.h;
-                        if (kb == 0) {
-                            if (!mbar_wait_bounded(tempty_bar(a), acc_phase[a] ^ 1u, p.wait_limit_ns, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * kBN);
-                        // rows 128..255 of the A stage start 16 KB in, in both A layouts
-                        const uint32_t sa_sub = sa + static_cast<uint32_t>(sub) * (kWABytes / 2);
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint64_t da = kAMN ? sdesc_mnmajor_sw128(sa_sub + kk * 2048, kMNBox)
-                                                     : sdesc_kmajor_sw128(sa_sub + kk * 32);
-                            const uint64_t db = kBMN ? sdesc_mnmajor_sw128(sb + kk * 2048, kMNBox)
-                                                     : sdesc_kmajor_sw128(sb + kk * 32);
-                            umma_f16_ss(d_tmem, da, db, kIdesc, (kb | kk) != 0 ? 1u : 0u);
-                        }
-                    }
-                    if (!ok) break;
-                    umma_commit(empty_bar(stage));
-                    if (++stage == kWStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                umma_commit(tfull_bar);
-                for (int a = 0; a < tc.halves; ++a) acc_phase[a] ^= 1u;
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                report_device_error(p.err, kKidGemmTc);
-            }
-            umma_commit(drain_bar);
-            mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, nullptr);
-        }
-    } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-        uint32_t tphase = 0;
-        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-            const TileCoord tc = decode_unit_wide(u, split_from, p);
-            if (tc.halves == 0) continue;
-            int ready = 0;
-            if (lane == 0) ready = mbar_wait_bounded(tfull_bar, tphase, p.wait_limit_ns, abort_flag);
-            ready = __shfl_sync(0xffffffffu, ready, 0);
-            if (!ready) {
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    report_device_error(p.err, kKidGemmTc);
-                }
-                break;
-            }
-            __syncwarp();
-            tc_fence_after();
-            for (int a = 0; a < tc.halves; ++a) {
-                const int sub = tc.halves == 2 ? a : tc.h;
-                const int64_t row = static_cast<int64_t>(tc.mb) * kWBM + sub * kBM + quarter * 32 + lane;
-                TC *crow = static_cast<TC *>(p.c) + static_cast<int64_t>(tc.bat) * p.sc + row * p.ldc;
-                const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                        static_cast<uint32_t>(a * kBN);
-#pragma unroll 1
-                for (int chunk = 0; chunk < kBN / 32; ++chunk) {
-                    uint32_t r[32];
-                    tmem_ld32(t_addr + chunk * 32, r);
-                    tmem_ld_wait();
-                    const int64_t col0 = static_cast<int64_t>(tc.nb) * kBN + chunk * 32;
-                    if (row < p.m && col0 < p.n) {
-                        if (p.c_vec_ok == 2 && col0 + 32 <= p.n) {
-                            // whole 32-byte sectors per store (this epilogue is not
-                            // overlapped with MMAs: its store rate shows directly),
-                            // streaming: C is not read again here, and lines marked
-                            // evict-first leave L2 (written back) while the GEMM still
-                            // runs instead of during the next kernel's reads
-#pragma unroll
-                            for (int v = 0; v < 2; ++v) {
-                                uint32_t o[8];
-#pragma unroll
-                                for (int q = 0; q < 8; ++q)
-                                    o[q] = pack2<TC>(__uint_as_float(r[16 * v + 2 * q]),
-                                                     __uint_as_float(r[16 * v + 2 * q + 1]));
-                                asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
-                                                 crow + col0 + 16 * v),
-                                             "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
-                                             "r"(o[6]), "r"(o[7])
-                                             : "memory");
-                            }
-                        } else if (p.c_vec_ok && col0 + 32 <= p.n) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                uint4 o;
-                                o.x = pack2<TC>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                                o.y = pack2<TC>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                                o.z = pack2<TC>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                                o.w = pack2<TC>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                                __stcs(dst + v, o);
-                            }
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                if (col0 + c < p.n) crow[col0 + c] = Elem<TC>::from_f(__uint_as_float(r[c]));
-                        }
-                    }
-                }
-                // this accumulator is stored: hand it back to the MMA issuer
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(a));
-            }
-            tphase ^= 1u;
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
-    }
-}
+constexpr int kWBM = 256;  // rows of a wide (CTA-pair) tile
 
 // ---------------------------------------------------------------------------
-// CTA-pair tiles (A and B both K-contiguous): 256 x 256 outputs per pair of
-// CTAs, computed by tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).
+// CTA-pair tiles: 256 x 256 outputs per pair of CTAs, computed by
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), for every layout of
+// the operands (K-contiguous: one 64 k x 128 row box per CTA and operand;
+// M/N-contiguous: two 64 x 64 boxes 8 KB apart, as in gemm_tc_kernel).
 // Each CTA of the pair holds 128 rows of the A tile and 128 rows of the B
 // tile per k-block (16 KB + 16 KB: half the operand bytes per SM of the
 // 256 x 256 single-CTA tile for the same MMA work per SM) and its tensor
@@ -637,7 +369,7 @@ constexpr uint32_t kPStageBytes = kPABytes + kPBBytes;
 constexpr uint32_t kPSmemBytes = kPStages * kPStageBytes + 256 + 1024;
 static_assert(kPStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
-template <typename TC, uint32_t kFmt>
+template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const GemmTcParams p) {
@@ -727,10 +459,20 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPStageBytes);
-                    const uint32_t sa = s0 + stage * kPStageBytes;
+                    const uint32_t sa = s0 + stage * kPStageBytes, sb = sa + kPABytes;
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
-                    tma_load_3d_pair(sa, &map_a, fb, kb * kBK, arow, abat);
-                    tma_load_3d_pair(sa + kPABytes, &map_b, fb, kb * kBK, brow, bbat);
+                    if (kAMN) {
+                        tma_load_3d_pair(sa, &map_a, fb, arow, kb * kBK, abat);
+                        tma_load_3d_pair(sa + kMNBox, &map_a, fb, arow + 64, kb * kBK, abat);
+                    } else {
+                        tma_load_3d_pair(sa, &map_a, fb, kb * kBK, arow, abat);
+                    }
+                    if (kBMN) {
+                        tma_load_3d_pair(sb, &map_b, fb, brow, kb * kBK, bbat);
+                        tma_load_3d_pair(sb + kMNBox, &map_b, fb, brow + 64, kb * kBK, bbat);
+                    } else {
+                        tma_load_3d_pair(sb, &map_b, fb, kb * kBK, brow, bbat);
+                    }
                     if (++stage == kPStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -748,8 +490,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- pair MMA issuer (even CTA) ----------------
-            constexpr uint32_t kIdesc = idesc_f16(kFmt, 2 * kBM, kBN);
-            constexpr uint32_t kIdescHalf = idesc_f16(kFmt, 2 * kBM, kBN / 2);
+            constexpr uint32_t kIdesc = idesc_f16(kFmt, 2 * kBM, kBN, kAMN ? 1u : 0u, kBMN ? 1u : 0u);
+            constexpr uint32_t kIdescHalf = idesc_f16(kFmt, 2 * kBM, kBN / 2, kAMN ? 1u : 0u, kBMN ? 1u : 0u);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t acc_phase[2] = {0u, 0u};
@@ -775,9 +517,13 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     tc_fence_after();
                     const uint32_t sa = s0 + stage * kPStageBytes, sb = sa + kPABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma_f16_ss_pair(d_tmem, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32),
-                                         idesc, (kb | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t da = kAMN ? sdesc_mnmajor_sw128(sa + kk * 2048, kMNBox)
+                                                 : sdesc_kmajor_sw128(sa + kk * 32);
+                        const uint64_t db = kBMN ? sdesc_mnmajor_sw128(sb + kk * 2048, kMNBox)
+                                                 : sdesc_kmajor_sw128(sb + kk * 32);
+                        umma_f16_ss_pair(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
                     umma_commit_pair_mc(empty_bar(stage), 0x3);  // the stage is free in both CTAs
                     if (++stage == kPStages) {
                         stage = 0;
@@ -875,7 +621,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     }
 }
 
-template <typename TC, uint32_t kFmt>
+template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
 cudaError_t tc_pair_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
                       cudaStream_t s) {
     static unsigned long long attr_set = 0;  // one bit per device
@@ -883,7 +629,7 @@ cudaError_t tc_pair_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTc
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel<TC, kFmt>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel<TC, kFmt, kAMN, kBMN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
@@ -903,34 +649,16 @@ cudaError_t tc_pair_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTc
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<TC, kFmt>, ma, mb, p);
-}
-
-template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
-cudaError_t tc_wide_t(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
-                      cudaStream_t s) {
-    static unsigned long long attr_set = 0;  // one bit per device
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_wide_kernel<TC, kFmt, kAMN, kBMN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set |= bit;
-    }
-    const int grid = 2 * p.num_tiles <= num_sms ? 2 * p.num_tiles : (p.num_tiles < num_sms ? p.num_tiles : num_sms);
-    gemm_tc_wide_kernel<TC, kFmt, kAMN, kBMN><<<grid, kThreads, kWSmemBytes, s>>>(ma, mb, p);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<TC, kFmt, kAMN, kBMN>, ma, mb, p);
 }
 
 template <typename TC, uint32_t kFmt>
-cudaError_t tc_wide_major(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
+cudaError_t tc_pair_major(const CUtensorMap &ma, const CUtensorMap &mb, const GemmTcParams &p, int num_sms,
                           cudaStream_t s) {
-    if (p.a_mn) return p.b_mn ? tc_wide_t<TC, kFmt, true, true>(ma, mb, p, num_sms, s)
-                              : tc_wide_t<TC, kFmt, true, false>(ma, mb, p, num_sms, s);
-    return p.b_mn ? tc_wide_t<TC, kFmt, false, true>(ma, mb, p, num_sms, s)
-                  : tc_wide_t<TC, kFmt, false, false>(ma, mb, p, num_sms, s);
+    if (p.a_mn) return p.b_mn ? tc_pair_t<TC, kFmt, true, true>(ma, mb, p, num_sms, s)
+                              : tc_pair_t<TC, kFmt, true, false>(ma, mb, p, num_sms, s);
+    return p.b_mn ? tc_pair_t<TC, kFmt, false, true>(ma, mb, p, num_sms, s)
+                  : tc_pair_t<TC, kFmt, false, false>(ma, mb, p, num_sms, s);
 }
 
 template <typename TC, uint32_t kFmt, bool kAMN, bool kBMN>
@@ -979,19 +707,9 @@ cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &
 
 cudaError_t launch_gemm_tc_pair(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                 const GemmTcParams &p, int num_sms, cudaStream_t s) {
-    if (p.a_mn || p.b_mn) return cudaErrorInvalidValue;
     switch (dt) {
-    case kF16: return tc_pair_t<__half, 0>(map_a, map_b, p, num_sms, s);
-    case kBF16: return tc_pair_t<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-cudaError_t launch_gemm_tc_wide(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                const GemmTcParams &p, int num_sms, cudaStream_t s) {
-    switch (dt) {
-    case kF16: return tc_wide_major<__half, 0>(map_a, map_b, p, num_sms, s);
-    case kBF16: return tc_wide_major<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
+    case kF16: return tc_pair_major<__half, 0>(map_a, map_b, p, num_sms, s);
+    case kBF16: return tc_pair_major<__nv_bfloat16, 1>(map_a, map_b, p, num_sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

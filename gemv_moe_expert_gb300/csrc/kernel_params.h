@@ -134,12 +134,9 @@ cudaError_t launch_gemm_simt(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_small(int dt, const GemmParams &p, cudaStream_t s);
 cudaError_t launch_gemm_tc(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                            const GemmTcParams &p, int num_sms, cudaStream_t s);
-// 256 x 256 tiles (two 128-row sub-tiles sharing the B tile); A's tensor map
-// box is gemm_tc_wide_block_m() rows when A is K-contiguous
-cudaError_t launch_gemm_tc_wide(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                const GemmTcParams &p, int num_sms, cudaStream_t s);
-// the same 256 x 256 tiles over CTA pairs (tcgen05 cta_group::2), A and B
-// K-contiguous only; both tensor maps with gemm_tc_block_m()-row boxes
+// 256 x 256 tiles (gemm_tc_wide_block_m() rows) over CTA pairs (tcgen05 cta_group::2); a
+// K-contiguous operand's tensor map has gemm_tc_block_m()-row boxes, an
+// M/N-contiguous one 64 x 64 boxes
 cudaError_t launch_gemm_tc_pair(int dt, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                 const GemmTcParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream_t s);
