@@ -84,7 +84,7 @@ constexpr uint32_t kWBase = kXStages * kXStageBytes;  // weight ring after the a
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kRingBytes = kWBase + kWStages * kWBytes;
-constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 4;
+constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 5;
 constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 8 * kNumBars + 16 + 1024;
 
 static_assert(kTailLo % 8 == 0 && kTailRows <= kTailLo && kTailLo + kTailRows <= kBM,
@@ -179,9 +179,11 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     auto xempty_bar = [&](int s) { return bar0 + 8u * (kXStages + s); };
     auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * kXStages + s); };
     auto wempty_bar = [&](int s) { return bar0 + 8u * (2 * kXStages + kWStages + s); };
-    const uint32_t tfull_bar = bar0 + 8u * (2 * kXStages + 2 * kWStages);
-    auto tempty_bar = [&](int h) { return tfull_bar + 8u * (1 + h); };  // one per accumulator half
-    const uint32_t drain_bar = tfull_bar + 24u;
+    // one full / empty pair per 256-column accumulator half
+    const uint32_t acc_bar0 = bar0 + 8u * (2 * kXStages + 2 * kWStages);
+    auto tfull_bar = [&](int h) { return acc_bar0 + 8u * h; };
+    auto tempty_bar = [&](int h) { return acc_bar0 + 8u * (2 + h); };
+    const uint32_t drain_bar = acc_bar0 + 32u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ uint32_t warp_tot[kThreads / 32];
@@ -202,7 +204,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             mbar_init(wfull_bar(s), 1);   // TMA thread's arrive + the copy's bytes
             mbar_init(wempty_bar(s), 1);  // MMA commit
         }
-        mbar_init(tfull_bar, 1);
+        mbar_init(tfull_bar(0), 1);
+        mbar_init(tfull_bar(1), 1);
         mbar_init(tempty_bar(0), 4);
         mbar_init(tempty_bar(1), 4);
         mbar_init(drain_bar, 1);
@@ -339,6 +342,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                                             sdesc_kmajor_sw128(s_hi + kk * 32), idesc_tail, (kb | kk) != 0 ? 1u : 0u);
                         }
                         umma_commit(wempty_bar(ws));
+                        // this half's accumulator is final: the epilogue may start on it
+                        // while the other half's last MMAs run
+                        if (kb == kblocks - 1) umma_commit(tfull_bar(h));
                         if (++ws == kWStages) {
                             ws = 0;
                             wph ^= 1u;
@@ -365,6 +371,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                             if (kSplit) umma_f16_ss(d_tmem, sdesc_kmajor_sw128(s_lo + kk * 32), dw, kIdesc, 1u);
                         }
                         umma_commit(wempty_bar(ws));
+                        // this half's accumulator is final: the epilogue may start on it
+                        // while the other half's last MMAs run
+                        if (kb == kblocks - 1) umma_commit(tfull_bar(h));
                         if (++ws == kWStages) {
                             ws = 0;
                             wph ^= 1u;
@@ -378,7 +387,6 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar);
                 for (int h = 0; h < g.halves; ++h) acc_phase[h] ^= 1u;
             }
             if (!ok) {
@@ -391,24 +399,36 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     } else if (warp < kProducerWarp0) {
         // ---------------- epilogue (warps 2..5) ----------------
         const int quarter = warp & 3;
-        uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-            const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
-            if (g.halves == 0) continue;
-            if (!warp_wait(tfull_bar, acc_phase, lim, abort_flag, lane)) {
+        uint32_t acc_phase = 0;  // bit h: phase of accumulator half h
+        bool ok = true;
+        // wait until accumulator half h of the current unit is final
+        auto wait_half = [&](int h) -> bool {
+            if (!warp_wait(tfull_bar(h), (acc_phase >> h) & 1u, lim, abort_flag, lane)) {
                 if (lane == 0) {
                     *abort_flag = 1;
                     report_device_error(p.err, kKidGroupedTc);
                 }
-                break;
+                return false;
             }
             tc_fence_after();
+            return true;
+        };
+        // all of half h is in registers or stored: hand it back to the MMA issuer
+        auto hand_back = [&](int h) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(h));
+        };
+        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
+            if (g.halves == 0) continue;
             if (g.tail) {
                 // lane = output column n0 + 128 q + 32 quarter + lane; TMEM column
                 // c (hi) + column kTailLo + c (lo) of accumulator q = routed row c
                 const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
                 const int64_t row_base = static_cast<int64_t>(g.e) * m + g.mb * kBM;
-                for (int q = 0; q < 2 * g.halves; ++q) {
+                for (int q = 0; q < 2 * g.halves && ok; ++q) {
+                    if (!(q & 1) && !(ok = wait_half(q >> 1))) break;
                     const int64_t j = static_cast<int64_t>(g.n0) + q * kBM + quarter * 32 + lane;
                     for (int c0 = 0; c0 < g.rows; c0 += 32) {
                         uint32_t vh[32], vl[32];
@@ -426,14 +446,10 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                             }
                         }
                     }
-                    if (q & 1) {
-                        // both accumulators of this 256-column half are read: hand it back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty_bar(q >> 1));
-                    }
+                    // both accumulators of this 256-column half are read
+                    if (q & 1) hand_back(q >> 1);
                 }
-                acc_phase ^= 1u;
+                acc_phase ^= (1u << g.halves) - 1u;
                 continue;
             }
             const int i = quarter * 32 + lane;
@@ -443,43 +459,53 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                                     : 0;
             float *orow = p.out + r * p.n;
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-            for (int chunk = 0; chunk < g.halves * (kBNH / 32); ++chunk) {
-                uint32_t v[32];
-                tmem_ld32(t_addr + chunk * 32, v);
-                tmem_ld_wait();
+            constexpr int kChunksPerHalf = kBNH / 32;
+            static_assert(kChunksPerHalf % 2 == 0, "chunks are read in pairs");
+            const int nch = g.halves * kChunksPerHalf;
+            auto store_chunk = [&](const uint32_t (&v)[32], int chunk) {
                 const int64_t j0 = static_cast<int64_t>(g.n0) + chunk * 32;
-                if (valid && j0 < p.n) {
-                    if (out_vec_ok == 2 && j0 + 32 <= p.n) {
-                        // whole 32-byte sectors per store: no partial-sector writes in L2
+                if (!valid || j0 >= p.n) return;
+                if (out_vec_ok == 2 && j0 + 32 <= p.n) {
+                    // whole 32-byte sectors per store: no partial-sector writes in L2
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            asm volatile(
-                                "st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + j0 + 8 * q),
-                                "r"(v[8 * q]), "r"(v[8 * q + 1]), "r"(v[8 * q + 2]), "r"(v[8 * q + 3]),
-                                "r"(v[8 * q + 4]), "r"(v[8 * q + 5]), "r"(v[8 * q + 6]), "r"(v[8 * q + 7])
-                                : "memory");
-                    } else if (out_vec_ok && j0 + 32 <= p.n) {
-                        float4 *dst = reinterpret_cast<float4 *>(orow + j0);
+                    for (int q = 0; q < 4; ++q)
+                        asm volatile(
+                            "st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + j0 + 8 * q),
+                            "r"(v[8 * q]), "r"(v[8 * q + 1]), "r"(v[8 * q + 2]), "r"(v[8 * q + 3]),
+                            "r"(v[8 * q + 4]), "r"(v[8 * q + 5]), "r"(v[8 * q + 6]), "r"(v[8 * q + 7])
+                            : "memory");
+                } else if (out_vec_ok && j0 + 32 <= p.n) {
+                    float4 *dst = reinterpret_cast<float4 *>(orow + j0);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            __stcs(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                        __uint_as_float(v[4 * q + 2]),
-                                                        __uint_as_float(v[4 * q + 3])));
-                    } else {
+                    for (int q = 0; q < 8; ++q)
+                        __stcs(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+                } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (j0 + c < p.n) orow[j0 + c] = __uint_as_float(v[c]);
-                    }
+                    for (int c = 0; c < 32; ++c)
+                        if (j0 + c < p.n) orow[j0 + c] = __uint_as_float(v[c]);
                 }
-                if ((chunk + 1) % (kBNH / 32) == 0) {
-                    // this accumulator half is in registers or stored: hand it back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(chunk / (kBNH / 32)));
+            };
+            // Two register buffers: chunk c + 1 is read from tensor memory while
+            // chunk c is stored.  A half goes back to the MMA issuer as soon as
+            // its last chunk has arrived in registers.
+            uint32_t va[32], vb[32];
+            if (!(ok = wait_half(0))) break;
+            tmem_ld32(t_addr, va);
+#pragma unroll 1
+            for (int chunk = 0; chunk < nch && ok; chunk += 2) {
+                tmem_ld_wait();  // va = chunk
+                tmem_ld32(t_addr + (chunk + 1) * 32, vb);
+                store_chunk(va, chunk);
+                tmem_ld_wait();  // vb = chunk + 1
+                if ((chunk + 2) % kChunksPerHalf == 0) hand_back((chunk + 1) / kChunksPerHalf);
+                if (chunk + 2 < nch) {
+                    if ((chunk + 2) % kChunksPerHalf == 0 && !(ok = wait_half((chunk + 2) / kChunksPerHalf))) break;
+                    tmem_ld32(t_addr + (chunk + 2) * 32, va);
                 }
+                store_chunk(vb, chunk + 1);
             }
-            acc_phase ^= 1u;
+            acc_phase ^= (1u << g.halves) - 1u;
         }
     } else {
         // ---------------- activation producers (warps 6..13) ----------------
