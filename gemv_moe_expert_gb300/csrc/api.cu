@@ -692,10 +692,11 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
     if (!resolve("gbmm_matmul_id_grouped")) return GBMM_ERR_KERNEL_UNAVAILABLE;
     mp.counts = scratch->expert_counts;
     mp.routed_rows = scratch->routed_rows;
-    // tensor-core grouped GEMM: bf16 weights read by TMA (16-byte aligned base,
-    // expert stride and rows), 16-byte aligned activation rows
+    // tensor-core grouped GEMM: bf16 or f16 weights read by TMA (16-byte aligned
+    // base, expert stride and rows), 16-byte aligned activation rows
     CUtensorMap map_w;
-    bool tc = weight_dtype == GBMM_BF16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
+    const bool w16 = weight_dtype == GBMM_BF16 || weight_dtype == GBMM_F16;
+    bool tc = w16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
               p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 && aligned(input, 16) &&
               p->n_experts <= static_cast<uint32_t>(grouped_tc_max_experts()) && p->n < (1u << 31) &&
               p->k < (1u << 31);
@@ -709,43 +710,24 @@ gbmm_status gbmm_matmul_id(const gbmm_matmul_id_params *p, gbmm_dtype weight_dty
         cuuint32_t wbox[3] = {static_cast<cuuint32_t>(bk), 256u, 1u};
         cuuint32_t estr[3] = {1u, 1u, 1u};
         tc = enc != nullptr &&
-             enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(weights), wdims, wstrides,
+             enc(&map_w, weight_dtype == GBMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 3, const_cast<void *>(weights), wdims, wstrides,
                  wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                  bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
-    // f16 weights: the Direct route's tensor-core kernel over the map's row lists
-    CUtensorMap map_f;
-    bool ftc = !tc && weight_dtype == GBMM_F16 && aligned(weights, 16) && p->expert_stride_bytes % 16 == 0 &&
-               p->expert_stride_bytes < (1ull << 40) && p->k % 8 == 0 && p->n < (1u << 31) && p->k < (1u << 31) &&
-               direct_tc_block_k() == 64;
-    if (ftc) {
-        PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-        cuuint64_t wdims[3] = {p->k, p->n, p->n_experts};
-        cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(p->k) * 2, p->expert_stride_bytes};
-        cuuint32_t wbox[3] = {static_cast<cuuint32_t>(direct_tc_block_k()),
-                              static_cast<cuuint32_t>(direct_tc_block_rows()), 1u};
-        cuuint32_t estr[3] = {1u, 1u, 1u};
-        ftc = enc != nullptr &&
-              enc(&map_f, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(weights), wdims, wstrides, wbox, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
-    if (tc || ftc) {
+    if (tc) {
         mp.err = device_error_word();
         if (mp.err == nullptr) return fail(GBMM_ERR_CUDA, "%s: device error word unavailable", fn);
     }
     st = after_launch(launch_matmul_id_map(mp, stream), "gbmm_matmul_id_map", stream);
     if (st != GBMM_OK) return st;
-    if (ftc) {
-        const int x_vec_ok = aligned(input, 16) && (mp.x_token_stride % 4 == 0) && (mp.x_slot_stride % 4 == 0);
-        st = after_launch(launch_matmul_id_grouped_direct_tc(weight_dtype, map_f, mp, x_vec_ok, stream),
-                          "gbmm_matmul_id_grouped_direct_tc", stream);
-    } else if (tc) {
+    if (tc) {
         // 2: 32-byte stores (rows 32-byte aligned), 1: 16-byte stores, 0: scalar
         const int out_vec_ok = (aligned(out, 32) && p->n % 8 == 0) ? 2 : (aligned(out, 16) && p->n % 4 == 0) ? 1 : 0;
         const int split = p->activation_precision == GBMM_ACT_SPLIT ? 1 : 0;
-        st = after_launch(launch_matmul_id_grouped_tc(map_w, mp, out_vec_ok, split, device_sm_count(), stream),
+        st = after_launch(launch_matmul_id_grouped_tc(map_w, mp, out_vec_ok, split, weight_dtype == GBMM_F16 ? 1 : 0,
+                                                      device_sm_count(), stream),
                           "gbmm_matmul_id_grouped_tc", stream);
     } else {
         st = after_launch(launch_matmul_id_grouped_simt(weight_dtype, mp, stream),

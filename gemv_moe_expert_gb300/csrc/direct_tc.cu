@@ -45,11 +45,6 @@
 //               k-block, split into bf16 hi / lo, write the swizzled K-major
 //               operand; after it: tcgen05.ld, hi + lo, f32 stores (a warp
 //               writes 32 consecutive outputs of a routed row)
-// The same kernel serves the GroupedPrefill route for f16 weights (the
-// grouped tcgen05 kernel takes bf16 only): there the map launch has already
-// written each expert's routed rows, so CTA (e, tile) reads expert e's count
-// and row list from the scratch instead of selecting from the ids, and the
-// map launch has written the zero rows.
 // Every mbarrier wait is bounded; a timeout is recorded in the device error
 // word, the CTA waits (bounded) for its own copies and MMAs, still takes part
 // in the cluster barriers, releases its TMEM and returns.
@@ -125,7 +120,7 @@ __device__ __forceinline__ const float *x_row_of(const MatmulIdParams &p, uint32
     return p.x + t * p.x_token_stride + s * p.x_slot_stride;
 }
 
-template <bool kF16, bool kFromMap>
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 3)
 direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams p, int ksplit, int tiles,
                  int x_vec_ok) {
@@ -179,15 +174,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
         tmem_alloc(smem_addr(ctl), kTmemCols);
         tmem_relinquish();
     }
-    if (kFromMap) {
-        // GroupedPrefill: the map launch wrote expert d's routed rows
-        if (threadIdx.x == 0) {
-            const uint32_t c0 = p.counts[d];
-            const uint32_t cm = c0 < static_cast<uint32_t>(p.m) ? c0 : static_cast<uint32_t>(p.m);
-            ctl[2] = cm > 0 ? static_cast<uint32_t>(d) : 0xffffffffu;
-            ctl[3] = cm;
-        }
-    } else {
+    {
         // ---- this CTA's expert: the d-th distinct in-range id, ascending ----
         for (int i = threadIdx.x; i < nwords; i += kThreads) emap[i] = 0u;
         __syncthreads();
@@ -246,9 +233,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
     const int e_sel = static_cast<int>(ctl[2]);
     const int cnt = static_cast<int>(ctl[3]);
     // routed row c of this CTA's expert
-    auto row_of = [&](int c) -> uint32_t {
-        return kFromMap ? p.routed_rows[static_cast<int64_t>(e_sel) * p.m + c] : rows_s[c];
-    };
+    auto row_of = [&](int c) -> uint32_t { return rows_s[c]; };
     const int passes = e_sel >= 0 ? (cnt + kBR - 1) / kBR : 0;
     const int kb_total = static_cast<int>((p.k + kBK - 1) / kBK);
     const int kb0 = static_cast<int>(static_cast<int64_t>(kb_total) * rank / ksplit);
@@ -494,7 +479,7 @@ direct_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams
     }
 
     // zero rows of out-of-range ids, once per output column
-    if (!kFromMap && d == 0 && rank == 0 && warp >= 2) {
+    if (d == 0 && rank == 0 && warp >= 2) {
         const int64_t j = static_cast<int64_t>(n0) + (warp & 3) * 32 + lane;
         if (j < p.n)
             for (int r = 0; r < n_ids; ++r)
@@ -532,7 +517,7 @@ int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows
 }
 
 namespace {
-template <bool kF16, bool kFromMap>
+template <bool kF16>
 cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int max_distinct, int ksplit,
                         int x_vec_ok, cudaStream_t s) {
     static unsigned long long attr_set = 0;  // one bit per device
@@ -540,7 +525,7 @@ cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int m
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(direct_tc_kernel<kF16, kFromMap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(direct_tc_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
@@ -560,7 +545,7 @@ cudaError_t direct_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int m
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, direct_tc_kernel<kF16, kFromMap>, map_w, p, ksplit, static_cast<int>(tiles),
+    return cudaLaunchKernelEx(&cfg, direct_tc_kernel<kF16>, map_w, p, ksplit, static_cast<int>(tiles),
                               x_vec_ok);
 }
 }  // namespace
@@ -571,18 +556,8 @@ cudaError_t launch_matmul_id_direct_tc(int wdt, const CUtensorMap &map_w, const 
         p.n_experts > kMaxExperts)
         return cudaErrorInvalidValue;
     switch (wdt) {
-    case kF16: return direct_tc_t<true, false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
-    case kBF16: return direct_tc_t<false, false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-cudaError_t launch_matmul_id_grouped_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
-                                               int x_vec_ok, cudaStream_t s) {
-    // one CTA per (expert, 128-row weight tile): the rows come from the map
-    if (p.n_experts < 1 || p.n_experts > 0x7fffffffLL) return cudaErrorInvalidValue;
-    switch (wdt) {
-    case kF16: return direct_tc_t<true, true>(map_w, p, static_cast<int>(p.n_experts), 1, x_vec_ok, s);
+    case kF16: return direct_tc_t<true>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
+    case kBF16: return direct_tc_t<false>(map_w, p, max_distinct, ksplit, x_vec_ok, s);
     default: return cudaErrorInvalidValue;
     }
 }

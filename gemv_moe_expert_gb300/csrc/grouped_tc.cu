@@ -1,5 +1,5 @@
 // grouped_tc.cu -- the grouped GEMM of the GroupedPrefill route on the sm_103a
-// tensor cores, for bf16 expert weights and f32 activations.
+// tensor cores, for bf16 or f16 expert weights and f32 activations.
 //
 // Semantics: mlx-native 0.13.0, src/ops/dense_matmul_id.rs, `dense_matmul_id`
 // (GroupedPrefill: per expert, the routed rows listed by the map dispatch
@@ -58,6 +58,16 @@
 // columns apart; the epilogue adds columns c and 64 + c of a lane (an output
 // column) and writes routed row c, a warp covering 32 consecutive outputs.
 // The arithmetic is the same bf16 hi + lo products as the other units.
+//
+// f16 weights.  One MMA takes one operand type, so with f16 weights the
+// activations are split into f16 hi + lo, and f16's range (largest finite
+// 65504, normal down to 2^-14) cannot hold every f32.  Each routed row of a
+// unit is therefore scaled by a power of two that puts its largest magnitude
+// over the whole k range in [2^14, 2^15) (the rule of the Direct kernel),
+// split, and its accumulator row multiplied back exactly in the epilogue.
+// The producers find the row maxima in a pass over the unit's rows before
+// its first k-block (8 lanes per row, 16-byte loads), and hand the inverse
+// scales to the epilogue through shared memory, double-buffered by unit.
 #include "device_common.cuh"
 
 namespace gbmm {
@@ -84,8 +94,8 @@ constexpr uint32_t kWBase = kXStages * kXStageBytes;  // weight ring after the a
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kRingBytes = kWBase + kWStages * kWBytes;
-constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 5;
-constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 8 * kNumBars + 16 + 1024;
+constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 9;  // + row-scale full / empty x 2 (f16 weights)
+constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 2 * kBM * 4 + 8 * kNumBars + 16 + 1024;
 
 static_assert(kTailLo % 8 == 0 && kTailRows <= kTailLo && kTailLo + kTailRows <= kBM,
               "a tail unit's hi and lo rows share the 128-row x_hi operand, in the same swizzle phase");
@@ -150,6 +160,36 @@ __device__ __forceinline__ float bf16_half(uint32_t packed, int half) {
     return __uint_as_float(half ? (packed & 0xffff0000u) : (packed << 16));
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// hi = round(a) (and lo = round(a - hi)) for a pair, in the weights' 16-bit type
+template <bool kF16, bool kSplit>
+__device__ __forceinline__ void split16(float a, float b, uint32_t &hi, uint32_t &lo) {
+    if (kF16) {
+        hi = pack_f16(a, b);
+        if (kSplit) {
+            const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+            lo = pack_f16(a - h.x, b - h.y);
+        }
+    } else {
+        hi = pack_bf16(a, b);
+        if (kSplit) lo = pack_bf16(a - bf16_half(hi, 0), b - bf16_half(hi, 1));
+    }
+}
+
+// power-of-two exponent that puts a row maximum mx in [2^14, 2^15), kept
+// within f32's normal range (0 for a zero row)
+__device__ __forceinline__ int row_scale_exp(float mx) {
+    if (!(mx > 0.f)) return 0;
+    const int eb = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu);
+    return min(126, max(-126, 141 - eb));
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
 // one lane waits, the warp follows its verdict (keeps the warp converged)
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
                                           volatile int *abort_flag, int lane) {
@@ -160,9 +200,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     return ready != 0;
 }
 
-// kSplit: activations as bf16 hi + lo (two MMAs per weight tile); without it
-// a single bf16 rounding (opt-in, half the tensor work).
-template <bool kSplit>
+// kSplit: activations as hi + lo (two MMAs per weight tile); without it a
+// single rounding (opt-in, half the tensor work).  kF16: f16 weights (row-
+// scaled f16 activations), else bf16.
+template <bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParams p, int out_vec_ok) {
     extern __shared__ uint8_t smem_raw[];
@@ -173,7 +214,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     // activation stage s at s_base + s*kXStageBytes (x_hi, x_lo); weight stage
     // s at s_base + kWBase + s*kWBytes
     uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kRingBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(prefix + kMaxExperts + 8);
+    float *unscale_s = reinterpret_cast<float *>(prefix + kMaxExperts + 8);  // [2][kBM], f16 weights
+    uint64_t *bars = reinterpret_cast<uint64_t *>(unscale_s + 2 * kBM);
     const uint32_t bar0 = smem_addr(bars);
     auto xfull_bar = [&](int s) { return bar0 + 8u * s; };
     auto xempty_bar = [&](int s) { return bar0 + 8u * (kXStages + s); };
@@ -184,6 +226,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     auto tfull_bar = [&](int h) { return acc_bar0 + 8u * h; };
     auto tempty_bar = [&](int h) { return acc_bar0 + 8u * (2 + h); };
     const uint32_t drain_bar = acc_bar0 + 32u;
+    // row scales of the unit with parity b written (producers) / read (epilogue)
+    auto sfull_bar = [&](int b) { return acc_bar0 + 40u + 8u * b; };
+    auto sempty_bar = [&](int b) { return acc_bar0 + 56u + 8u * b; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ uint32_t warp_tot[kThreads / 32];
@@ -209,6 +254,10 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         mbar_init(tempty_bar(0), 4);
         mbar_init(tempty_bar(1), 4);
         mbar_init(drain_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sfull_bar(b), 8);   // one arrive per producer warp
+            mbar_init(sempty_bar(b), 4);  // one arrive per epilogue warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -306,7 +355,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t kIdesc = idesc_f16(1u, kBM, kBNH);  // bf16 x bf16 -> f32
+            constexpr uint32_t kFmt = kF16 ? 0u : 1u;                 // f16 or bf16 operands
+            constexpr uint32_t kIdesc = idesc_f16(kFmt, kBM, kBNH);  // 16-bit x 16-bit -> f32
             int xs = 0, ws = 0;
             uint32_t xph = 0, wph = 0, acc_phase[2] = {0u, 0u};
             bool ok = true;
@@ -314,7 +364,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
                 if (g.halves == 0) continue;
                 // tail unit: weights as A (M = 128), the routed rows as B (N rows)
-                const uint32_t idesc_tail = idesc_f16(1u, kBM, tail_n<kSplit>(g.rows));
+                const uint32_t idesc_tail = idesc_f16(kFmt, kBM, tail_n<kSplit>(g.rows));
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
                     if (!mbar_wait_bounded(xfull_bar(xs), xph, lim, abort_flag)) {
                         ok = false;
@@ -419,9 +469,29 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(h));
         };
+        uint32_t uc = 0;  // units with work so far (row-scale buffer uc & 1)
         for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
             const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
             if (g.halves == 0) continue;
+            const int sb = static_cast<int>(uc & 1u);
+            const float *unscale = unscale_s + sb * kBM;
+            if (kF16) {
+                if (!(ok = warp_wait(sfull_bar(sb), (uc >> 1) & 1u, lim, abort_flag, lane))) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_device_error(p.err, kKidGroupedTc);
+                    }
+                    break;
+                }
+            }
+            // this unit's row scales are read: the producers may refill the buffer
+            auto release_scales = [&]() {
+                if (kF16) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sempty_bar(sb));
+                }
+                ++uc;
+            };
             if (g.tail) {
                 // lane = output column n0 + 128 q + 32 quarter + lane; TMEM column
                 // c (hi) + column kTailLo + c (lo) of accumulator q = routed row c
@@ -440,8 +510,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                         for (int c = 0; c < 32; ++c) {
                             const uint32_t r = __shfl_sync(0xffffffffu, my_r, c);
                             if (c0 + c < g.rows && j < p.n) {
-                                const float v = kSplit ? __uint_as_float(vh[c]) + __uint_as_float(vl[c])
-                                                       : __uint_as_float(vh[c]);
+                                float v = kSplit ? __uint_as_float(vh[c]) + __uint_as_float(vl[c])
+                                                 : __uint_as_float(vh[c]);
+                                if (kF16) v *= unscale[c0 + c];
                                 __stcs(p.out + static_cast<int64_t>(r) * p.n + j, v);
                             }
                         }
@@ -450,6 +521,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     if (q & 1) hand_back(q >> 1);
                 }
                 acc_phase ^= (1u << g.halves) - 1u;
+                release_scales();
                 continue;
             }
             const int i = quarter * 32 + lane;
@@ -458,13 +530,18 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                                                                          g.mb * kBM + i])
                                     : 0;
             float *orow = p.out + r * p.n;
+            const float rs = kF16 ? unscale[i] : 1.f;  // exact power of two
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
             constexpr int kChunksPerHalf = kBNH / 32;
             static_assert(kChunksPerHalf % 2 == 0, "chunks are read in pairs");
             const int nch = g.halves * kChunksPerHalf;
-            auto store_chunk = [&](const uint32_t (&v)[32], int chunk) {
+            auto store_chunk = [&](uint32_t (&v)[32], int chunk) {
                 const int64_t j0 = static_cast<int64_t>(g.n0) + chunk * 32;
                 if (!valid || j0 >= p.n) return;
+                if (kF16) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * rs);
+                }
                 if (out_vec_ok == 2 && j0 + 32 <= p.n) {
                     // whole 32-byte sectors per store: no partial-sector writes in L2
 #pragma unroll
@@ -506,6 +583,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 store_chunk(vb, chunk + 1);
             }
             acc_phase ^= (1u << g.halves) - 1u;
+            release_scales();
         }
     } else {
         // ---------------- activation producers (warps 6..13) ----------------
@@ -519,6 +597,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         const uint64_t pol = policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
+        uint32_t uc = 0;  // units with work so far (row-scale buffer uc & 1)
         bool ok = true;
         for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
             const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
@@ -534,6 +613,64 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     src[q] = p.x + tok * p.x_token_stride + slot * p.x_slot_stride + sub * 8;
                 }
             }
+            // f16 weights: each row's scale from its largest magnitude over k
+            float scl[kRowsPerProducer];
+#pragma unroll
+            for (int q = 0; q < kRowsPerProducer; ++q) scl[q] = 1.f;
+            if (kF16) {
+                float mx[kRowsPerProducer];
+#pragma unroll
+                for (int q = 0; q < kRowsPerProducer; ++q) mx[q] = 0.f;
+                for (int kb = 0; kb < kblocks; kb += 2) {
+                    float4 a[2][kRowsPerProducer][2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const bool in_k = kb + t < kblocks && static_cast<int64_t>(kb + t) * kBK + sub * 8 < p.k;
+#pragma unroll
+                        for (int q = 0; q < kRowsPerProducer; ++q) {
+                            if (in_k && src[q] != nullptr) {
+                                a[t][q][0] = ld_f4_policy(src[q] + static_cast<int64_t>(kb + t) * kBK, pol);
+                                a[t][q][1] = ld_f4_policy(src[q] + static_cast<int64_t>(kb + t) * kBK + 4, pol);
+                            } else {
+                                a[t][q][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                a[t][q][1] = a[t][q][0];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int q = 0; q < kRowsPerProducer; ++q)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                mx[q] = fmaxf(mx[q], fmaxf(fmaxf(fabsf(a[t][q][h].x), fabsf(a[t][q][h].y)),
+                                                           fmaxf(fabsf(a[t][q][h].z), fabsf(a[t][q][h].w))));
+                }
+                // the 8 lanes of a row (sub = lane & 7) combine their maxima
+#pragma unroll
+                for (int q = 0; q < kRowsPerProducer; ++q)
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
+                const int sb = static_cast<int>(uc & 1u);
+                // the epilogue has read this buffer's scales of two units ago
+                if (!warp_wait(sempty_bar(sb), ((uc >> 1) & 1u) ^ 1u, lim, abort_flag, lane)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_device_error(p.err, kKidGroupedTc);
+                    }
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int q = 0; q < kRowsPerProducer; ++q) {
+                    const int se = row_scale_exp(mx[q]);
+                    scl[q] = pow2f(se);
+                    if (sub == 0) unscale_s[sb * kBM + rsub + 32 * q] = pow2f(-se);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfull_bar(sb));
+            }
+            ++uc;
             float4 ring0[kRowsPerProducer][2], ring1[kRowsPerProducer][2], ring2[kRowsPerProducer][2];
             auto issue = [&](float4 (&buf)[kRowsPerProducer][2], int kb) {
                 // L2 prefetch of the rows' segment kXPrefetch k-blocks further on:
@@ -576,9 +713,10 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        hi[h] = pack_bf16(f[2 * h], f[2 * h + 1]);
-                        if (kSplit)
-                            lo[h] = pack_bf16(f[2 * h] - bf16_half(hi[h], 0), f[2 * h + 1] - bf16_half(hi[h], 1));
+                        if (kF16)
+                            split16<true, kSplit>(f[2 * h] * scl[q], f[2 * h + 1] * scl[q], hi[h], lo[h]);
+                        else
+                            split16<false, kSplit>(f[2 * h], f[2 * h + 1], hi[h], lo[h]);
                     }
                     // 128-byte swizzle: 16-byte chunk c of row i sits at chunk c ^ (i % 8)
                     const uint32_t off = static_cast<uint32_t>(i) * 128u +
@@ -630,7 +768,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 }  // namespace
 
 namespace {
-template <bool kSplit>
+template <bool kSplit, bool kF16>
 cudaError_t grouped_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok, int num_sms,
                          cudaStream_t s) {
     static unsigned long long attr_set = 0;
@@ -638,20 +776,23 @@ cudaError_t grouped_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int 
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<kSplit>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<kSplit, kF16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    grouped_tc_kernel<kSplit><<<num_sms, kThreads, kSmemBytes, s>>>(map_w, p, out_vec_ok);
+    grouped_tc_kernel<kSplit, kF16><<<num_sms, kThreads, kSmemBytes, s>>>(map_w, p, out_vec_ok);
     return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
-                                        int split, int num_sms, cudaStream_t s) {
-    return split ? grouped_tc_t<true>(map_w, p, out_vec_ok, num_sms, s)
-                 : grouped_tc_t<false>(map_w, p, out_vec_ok, num_sms, s);
+                                        int split, int f16, int num_sms, cudaStream_t s) {
+    if (f16)
+        return split ? grouped_tc_t<true, true>(map_w, p, out_vec_ok, num_sms, s)
+                     : grouped_tc_t<false, true>(map_w, p, out_vec_ok, num_sms, s);
+    return split ? grouped_tc_t<true, false>(map_w, p, out_vec_ok, num_sms, s)
+                 : grouped_tc_t<false, false>(map_w, p, out_vec_ok, num_sms, s);
 }
 
 int grouped_tc_max_experts() { return kMaxExperts; }

@@ -143,7 +143,7 @@ cudaError_t launch_matmul_id_direct(int wdt, const MatmulIdParams &p, cudaStream
 cudaError_t launch_matmul_id_map(const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_simt(int wdt, const MatmulIdParams &p, cudaStream_t s);
 cudaError_t launch_matmul_id_grouped_tc(const CUtensorMap &map_w, const MatmulIdParams &p, int out_vec_ok,
-                                        int split, int num_sms, cudaStream_t s);
+                                        int split, int f16, int num_sms, cudaStream_t s);
 cudaError_t launch_bounded_wait_test(uint32_t *err, uint64_t limit_ns, cudaStream_t s);
 int grouped_tc_max_experts();
 // Direct route on the tensor cores (direct_tc.cu): bf16 or f16 weights
@@ -153,10 +153,6 @@ int grouped_tc_max_experts();
 cudaError_t launch_matmul_id_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
                                        int max_distinct, int ksplit, int x_vec_ok, cudaStream_t s);
 int direct_tc_split(int64_t n, int64_t k, int64_t max_distinct, int64_t max_rows_per_expert, int num_sms);
-// GroupedPrefill with f16 weights on the same kernel: one CTA per (expert,
-// tile), the routed rows read from the map's scratch (counts, routed_rows)
-cudaError_t launch_matmul_id_grouped_direct_tc(int wdt, const CUtensorMap &map_w, const MatmulIdParams &p,
-                                               int x_vec_ok, cudaStream_t s);
 int direct_tc_max_ids();
 int direct_tc_max_experts();
 int direct_tc_block_rows();

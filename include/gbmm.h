@@ -154,23 +154,28 @@ typedef struct gbmm_matmul_id_params {
     uint32_t route;        /* GBMM_ROUTE_* */
     uint64_t expert_stride_bytes; /* bytes from expert e to expert e+1 */
     /* GBMM_ACT_* (an extension of this library; zero = the pages' f32
-     * activation product).  Only the GroupedPrefill route with bf16 weights on
-     * the tensor cores reads it; elsewhere every value computes in f32. */
+     * activation product).  Only the GroupedPrefill route with bf16 or f16
+     * weights on the tensor cores reads it; elsewhere every value computes in
+     * f32. */
     uint32_t activation_precision;
     uint32_t reserved;     /* must be 0 */
 } gbmm_matmul_id_params;
 
 /*
- * Activation precision of the tensor-core grouped GEMM (bf16 weights, f32
- * activations).  Tensor cores multiply bf16 pairs, so the f32 activations
- * must be rounded:
- *   GBMM_ACT_SPLIT (default): x = hi + lo with hi = bf16(x), lo = bf16(x - hi),
- *     both multiplied by the weights -- activation error <= 2^-16 |x|, the
- *     product is f32-accurate and every element meets 2e-3 * sum|w||x|.
- *   GBMM_ACT_BF16: x rounded once to bf16, half the tensor work -- activation
- *     error <= 2^-8 |x|, so an element can differ from the f32 product by up
- *     to ~2^-8 * sum|w||x| (about 3.9e-3, above the 2e-3 bound when all
- *     products share a sign; far below it for zero-mean data).
+ * Activation precision of the tensor-core grouped GEMM (bf16 or f16 weights,
+ * f32 activations).  Tensor cores multiply pairs of one 16-bit type, so the
+ * f32 activations must be rounded to the weights' type (for f16 weights each
+ * routed row first scaled by a power of two that puts its largest magnitude
+ * in [2^14, 2^15), and the result scaled back exactly):
+ *   GBMM_ACT_SPLIT (default): x = hi + lo with hi = round(x), lo = round(x - hi),
+ *     both multiplied by the weights -- activation error <= 2^-16 |x| (bf16),
+ *     2^-22 |x| (f16), the product is f32-accurate and every element meets
+ *     2e-3 * sum|w||x|.
+ *   GBMM_ACT_BF16: x rounded once, half the tensor work -- activation error
+ *     <= 2^-8 |x| for bf16 weights, so an element can differ from the f32
+ *     product by up to ~2^-8 * sum|w||x| (about 3.9e-3, above the 2e-3 bound
+ *     when all products share a sign; far below it for zero-mean data); for
+ *     f16 weights <= 2^-11 |x|, inside the bound.
  */
 enum { GBMM_ACT_SPLIT = 0, GBMM_ACT_BF16 = 1 };
 
@@ -383,8 +388,7 @@ GBMM_API void gbmm_test_reset_launch_count(void);
  * "gbmm_gemm_tc", "gbmm_gemm_simt", "gbmm_gemm_small", "gbmm_gemv_stream",
  * "gbmm_gemv_rowdot", "gbmm_gemv_coldot", "gbmm_gemv_tc", "gbmm_fill_zero",
  * "gbmm_matmul_id_direct", "gbmm_matmul_id_direct_tc", "gbmm_matmul_id_map",
- * "gbmm_matmul_id_grouped_tc", "gbmm_matmul_id_grouped_direct_tc",
- * "gbmm_matmul_id_grouped_simt", and "gbmm_bounded_wait_test" for the wait test below. */
+ * "gbmm_matmul_id_grouped_tc", "gbmm_matmul_id_grouped_simt", and "gbmm_bounded_wait_test" for the wait test below. */
 GBMM_API const char *gbmm_test_last_kernel(void);
 
 /*

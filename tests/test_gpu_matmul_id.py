@@ -237,7 +237,7 @@ def test_matmul_id_parity_small(oracle_mod, wdtype, route, layout):
                                 route=route, input_layout=layout, stride_pad_elems=8, seed=3)
     Run(case).call().check(oracle_mod)
     if route == 1:
-        want = {"bf16": "gbmm_matmul_id_grouped_tc", "f16": "gbmm_matmul_id_grouped_direct_tc",
+        want = {"bf16": "gbmm_matmul_id_grouped_tc", "f16": "gbmm_matmul_id_grouped_tc",
                 "f32": "gbmm_matmul_id_grouped_simt"}[wdtype]
         assert gb.gbmm_test_last_kernel() == want
 
@@ -459,19 +459,45 @@ def test_grouped_ffma_row_block_sizes(oracle_mod, wdtype):
     r.check_map(oracle_mod)
 
 
-def test_grouped_f16_tensor_core_passes_and_range(oracle_mod):
-    """GroupedPrefill with f16 weights on the tensor cores (the Direct kernel
-    reading the map's row lists): 1200 routed rows over 6 experts (up to ~13
-    passes of 16 rows per expert), ragged n and k, Slotted rows of magnitude
-    1e20, 1e-20 and 7e4 mixed in; every output and the map."""
+@pytest.mark.parametrize("precision", [0, 1])
+def test_grouped_f16_tensor_core_row_scales(oracle_mod, precision):
+    """GroupedPrefill with f16 weights on the grouped tensor-core kernel: each
+    routed row of a unit is scaled by a power of two from its largest magnitude
+    over the whole k range before the f16 split.  1200 Slotted routed rows over
+    6 experts (row blocks of 128 and a last block per expert, ragged n and k)
+    with rows of magnitude 1e30, 1e-30, 7e4 (above f16's largest finite
+    value), zero rows and rows spanning 2^24 mixed in; every output and the
+    map.  precision 1 is the opt-in single rounding, which for f16 (11
+    significant bits) still meets 2e-3 * sum|w||x|."""
     m, top_k, E, n, k = 300, 4, 6, 264, 1000
     c = synth.matmul_id_case("f16grouped", "f16", m, n, k, top_k, E, route=1, input_layout=1, seed=23)
     rows = c.x.reshape(m * top_k, k)
-    rows[::7] *= np.float32(1e20)
-    rows[3::11] *= np.float32(1e-20)
+    rows[::7] *= np.float32(1e30)
+    rows[3::11] *= np.float32(1e-30)
     rows[5::13] *= np.float32(7e4)
+    rows[9::17] = 0.0
+    rows[2::19] *= np.exp2(np.linspace(-12, 12, k)).astype(np.float32)
+    r = Run(c, precision=precision).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+    r.check(oracle_mod)
+    r.check_map(oracle_mod)
+
+
+@pytest.mark.parametrize("count", [1, 17, 64, 65, 128, 200])
+def test_grouped_f16_tail_and_full_blocks(oracle_mod, count):
+    """f16 weights: an expert list of `count` routed rows (tail units for at
+    most 64 rows in the last block, full blocks above) next to a second
+    expert of 100 rows, rows of mixed magnitude; every output."""
+    sizes = [count, 100]
+    ids = np.concatenate([np.full(c_, e, dtype=np.uint32) for e, c_ in enumerate(sizes)])
+    ids = np.random.default_rng(count).permutation(ids).reshape(-1, 1)
+    m, E = ids.shape[0], len(sizes)
+    c = synth.matmul_id_case(f"f16tail{count}", "f16", m, 600, 264, 1, E, route=1, ids=ids, seed=count)
+    rows = c.x.reshape(m, 264)
+    rows[::5] *= np.float32(3e5)
+    rows[1::6] *= np.float32(2e-9)
     r = Run(c).call()
-    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_direct_tc"
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
     r.check(oracle_mod)
 
 
