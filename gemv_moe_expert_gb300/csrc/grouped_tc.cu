@@ -65,9 +65,11 @@
 // unit is therefore scaled by a power of two that puts its largest magnitude
 // over the whole k range in [2^14, 2^15) (the rule of the Direct kernel),
 // split, and its accumulator row multiplied back exactly in the epilogue.
-// The producers find the row maxima in a pass over the unit's rows before
-// its first k-block (8 lanes per row, 16-byte loads), and hand the inverse
-// scales to the epilogue through shared memory, double-buffered by unit.
+// The row maxima (8 lanes per row, 16-byte loads) of a CTA's first unit are
+// found by the producer warps before its first k-block, those of every later
+// unit by the epilogue warps, which are idle while the tensor cores work on
+// the unit before it; the scale exponents pass through shared memory,
+// double-buffered by unit.
 #include "device_common.cuh"
 
 namespace gbmm {
@@ -94,7 +96,7 @@ constexpr uint32_t kWBase = kXStages * kXStageBytes;  // weight ring after the a
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kRingBytes = kWBase + kWStages * kWBytes;
-constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 9;  // + row-scale full / empty x 2 (f16 weights)
+constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 10;  // + row-scale barriers (f16 weights)
 constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 2 * kBM * 4 + 8 * kNumBars + 16 + 1024;
 
 static_assert(kTailLo % 8 == 0 && kTailRows <= kTailLo && kTailLo + kTailRows <= kBM,
@@ -190,6 +192,13 @@ __device__ __forceinline__ int row_scale_exp(float mx) {
 
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
+// Parity of the row-scale full barrier of buffer j & 1 for the CTA's j-th
+// unit (j >= 1): buffer 1 completes for j = 1, 3, 5, ..., buffer 0 for
+// j = 2, 4, ... (the first unit's scales use their own barrier).
+__device__ __forceinline__ uint32_t sfull_parity(uint32_t j) {
+    return (j & 1u) ? ((j >> 1) & 1u) : (((j >> 1) & 1u) ^ 1u);
+}
+
 // one lane waits, the warp follows its verdict (keeps the warp converged)
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
                                           volatile int *abort_flag, int lane) {
@@ -214,8 +223,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     // activation stage s at s_base + s*kXStageBytes (x_hi, x_lo); weight stage
     // s at s_base + kWBase + s*kWBytes
     uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kRingBytes);
-    float *unscale_s = reinterpret_cast<float *>(prefix + kMaxExperts + 8);  // [2][kBM], f16 weights
-    uint64_t *bars = reinterpret_cast<uint64_t *>(unscale_s + 2 * kBM);
+    int *rexp_s = reinterpret_cast<int *>(prefix + kMaxExperts + 8);  // [2][kBM] row scale exponents (f16)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rexp_s + 2 * kBM);
     const uint32_t bar0 = smem_addr(bars);
     auto xfull_bar = [&](int s) { return bar0 + 8u * s; };
     auto xempty_bar = [&](int s) { return bar0 + 8u * (kXStages + s); };
@@ -226,9 +235,12 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     auto tfull_bar = [&](int h) { return acc_bar0 + 8u * h; };
     auto tempty_bar = [&](int h) { return acc_bar0 + 8u * (2 + h); };
     const uint32_t drain_bar = acc_bar0 + 32u;
-    // row scales of the unit with parity b written (producers) / read (epilogue)
+    // f16 weights: row scales of the CTA's j-th unit, in buffer j & 1, written
+    // (by the producers for j = 0: s0_bar; by the epilogue after: sfull_bar)
+    // and read by the producers (sempty_bar)
     auto sfull_bar = [&](int b) { return acc_bar0 + 40u + 8u * b; };
     auto sempty_bar = [&](int b) { return acc_bar0 + 56u + 8u * b; };
+    const uint32_t s0_bar = acc_bar0 + 72u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ uint32_t warp_tot[kThreads / 32];
@@ -255,9 +267,10 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         mbar_init(tempty_bar(1), 4);
         mbar_init(drain_bar, 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(sfull_bar(b), 8);   // one arrive per producer warp
-            mbar_init(sempty_bar(b), 4);  // one arrive per epilogue warp
+            mbar_init(sfull_bar(b), 4);   // one arrive per epilogue warp
+            mbar_init(sempty_bar(b), 8);  // one arrive per producer warp
         }
+        mbar_init(s0_bar, 8);  // one arrive per producer warp
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -469,14 +482,72 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(h));
         };
-        uint32_t uc = 0;  // units with work so far (row-scale buffer uc & 1)
-        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        // the CTA's next unit with work after u (num_units: none)
+        auto next_unit = [&](int u) -> int {
+            for (u += gridDim.x; u < num_units; u += gridDim.x)
+                if (decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n).halves > 0) return u;
+            return num_units;
+        };
+        // f16 weights: the scale exponents of unit u (the CTA's j-th unit with
+        // work) into buffer j & 1, each warp taking rows 16 g + 4 quarter +
+        // lane / 8 (g < 8), 8 lanes per row with 16 loads of 16 bytes in flight
+        const uint64_t xpol = policy_evict_last();
+        auto row_scales = [&](int u, uint32_t j) -> bool {
             const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
-            if (g.halves == 0) continue;
+            const int b = static_cast<int>(j & 1u);
+            // the producers have read buffer b's scales of unit j - 2
+            if (!warp_wait(sempty_bar(b), ((j >> 1) & 1u) ^ 1u, lim, abort_flag, lane)) return false;
+            const int sub = lane & 7;
+            for (int g4 = 0; g4 < kBM / 16; ++g4) {
+                const int i = 16 * g4 + 4 * quarter + (lane >> 3);
+                if (16 * g4 >= g.rows) break;  // warp-uniform: no row of this group or later
+                const float *src = nullptr;
+                if (i < g.rows) {
+                    const uint32_t r = p.routed_rows[static_cast<int64_t>(g.e) * m + g.mb * kBM + i];
+                    const int64_t tok = r / p.top_k, slot = r % p.top_k;
+                    src = p.x + tok * p.x_token_stride + slot * p.x_slot_stride + sub * 4;
+                }
+                float mx = 0.f;
+                for (int64_t c0 = 0; c0 < p.k; c0 += 32 * 16) {
+                    float4 a[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int64_t kk = c0 + 32 * t;
+                        a[t] = (src != nullptr && kk + sub * 4 < p.k) ? ld_f4_policy(src + kk, xpol)
+                                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a[t].x), fabsf(a[t].y)), fmaxf(fabsf(a[t].z), fabsf(a[t].w))));
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (sub == 0) rexp_s[b * kBM + i] = row_scale_exp(mx);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sfull_bar(b));
+            return true;
+        };
+        uint32_t uc = 0;  // units with work so far (row-scale buffer uc & 1)
+        int u = blockIdx.x;
+        while (u < num_units && decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n).halves == 0)
+            u += gridDim.x;
+        int u1 = u < num_units ? next_unit(u) : num_units;
+        // unit 1's scales while the producers find unit 0's
+        if (kF16 && u1 < num_units && !(ok = row_scales(u1, 1)) && lane == 0) {
+            *abort_flag = 1;
+            report_device_error(p.err, kKidGroupedTc);
+        }
+        for (; u < num_units && ok;) {
+            const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
             const int sb = static_cast<int>(uc & 1u);
-            const float *unscale = unscale_s + sb * kBM;
+            const int *rexp = rexp_s + sb * kBM;
             if (kF16) {
-                if (!(ok = warp_wait(sfull_bar(sb), (uc >> 1) & 1u, lim, abort_flag, lane))) {
+                // this unit's scales, complete from all their writers
+                const bool ready = uc == 0 ? warp_wait(s0_bar, 0u, lim, abort_flag, lane)
+                                           : warp_wait(sfull_bar(sb), sfull_parity(uc), lim, abort_flag, lane);
+                ok = ready;
+                if (!ok) {
                     if (lane == 0) {
                         *abort_flag = 1;
                         report_device_error(p.err, kKidGroupedTc);
@@ -484,13 +555,17 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     break;
                 }
             }
-            // this unit's row scales are read: the producers may refill the buffer
-            auto release_scales = [&]() {
-                if (kF16) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sempty_bar(sb));
+            // after this unit's rows are stored: the scales of the unit after
+            // the next one (its buffer is this unit's), while the next runs
+            auto advance = [&]() {
+                const int u2 = u1 < num_units ? next_unit(u1) : num_units;
+                if (kF16 && u2 < num_units && !(ok = row_scales(u2, uc + 2)) && lane == 0) {
+                    *abort_flag = 1;
+                    report_device_error(p.err, kKidGroupedTc);
                 }
                 ++uc;
+                u = u1;
+                u1 = u2;
             };
             if (g.tail) {
                 // lane = output column n0 + 128 q + 32 quarter + lane; TMEM column
@@ -512,7 +587,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                             if (c0 + c < g.rows && j < p.n) {
                                 float v = kSplit ? __uint_as_float(vh[c]) + __uint_as_float(vl[c])
                                                  : __uint_as_float(vh[c]);
-                                if (kF16) v *= unscale[c0 + c];
+                                if (kF16) v *= pow2f(-rexp[c0 + c]);
                                 __stcs(p.out + static_cast<int64_t>(r) * p.n + j, v);
                             }
                         }
@@ -521,7 +596,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     if (q & 1) hand_back(q >> 1);
                 }
                 acc_phase ^= (1u << g.halves) - 1u;
-                release_scales();
+                advance();
                 continue;
             }
             const int i = quarter * 32 + lane;
@@ -530,7 +605,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                                                                          g.mb * kBM + i])
                                     : 0;
             float *orow = p.out + r * p.n;
-            const float rs = kF16 ? unscale[i] : 1.f;  // exact power of two
+            const float rs = kF16 ? pow2f(-rexp[i]) : 1.f;  // exact power of two
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
             constexpr int kChunksPerHalf = kBNH / 32;
             static_assert(kChunksPerHalf % 2 == 0, "chunks are read in pairs");
@@ -583,7 +658,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 store_chunk(vb, chunk + 1);
             }
             acc_phase ^= (1u << g.halves) - 1u;
-            release_scales();
+            advance();
         }
     } else {
         // ---------------- activation producers (warps 6..13) ----------------
@@ -617,7 +692,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             float scl[kRowsPerProducer];
 #pragma unroll
             for (int q = 0; q < kRowsPerProducer; ++q) scl[q] = 1.f;
-            if (kF16) {
+            if (kF16 && uc == 0) {
+                // the CTA's first unit: its row maxima over k, before its first k-block
                 float mx[kRowsPerProducer];
 #pragma unroll
                 for (int q = 0; q < kRowsPerProducer; ++q) mx[q] = 0.f;
@@ -648,12 +724,22 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 }
                 // the 8 lanes of a row (sub = lane & 7) combine their maxima
 #pragma unroll
-                for (int q = 0; q < kRowsPerProducer; ++q)
+                for (int q = 0; q < kRowsPerProducer; ++q) {
 #pragma unroll
                     for (int o = 1; o < 8; o <<= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
+                    const int se = row_scale_exp(mx[q]);
+                    scl[q] = pow2f(se);
+                    if (sub == 0) rexp_s[rsub + 32 * q] = se;  // buffer 0, for the epilogue
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(s0_bar);
+                    mbar_arrive(sempty_bar(0));  // scales kept in registers
+                }
+            } else if (kF16) {
+                // the epilogue warps have found this unit's row scales
                 const int sb = static_cast<int>(uc & 1u);
-                // the epilogue has read this buffer's scales of two units ago
-                if (!warp_wait(sempty_bar(sb), ((uc >> 1) & 1u) ^ 1u, lim, abort_flag, lane)) {
+                if (!warp_wait(sfull_bar(sb), sfull_parity(uc), lim, abort_flag, lane)) {
                     if (lane == 0) {
                         *abort_flag = 1;
                         report_device_error(p.err, kKidGroupedTc);
@@ -662,13 +748,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     break;
                 }
 #pragma unroll
-                for (int q = 0; q < kRowsPerProducer; ++q) {
-                    const int se = row_scale_exp(mx[q]);
-                    scl[q] = pow2f(se);
-                    if (sub == 0) unscale_s[sb * kBM + rsub + 32 * q] = pow2f(-se);
-                }
+                for (int q = 0; q < kRowsPerProducer; ++q) scl[q] = pow2f(rexp_s[sb * kBM + rsub + 32 * q]);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sfull_bar(sb));
+                if (lane == 0) mbar_arrive(sempty_bar(sb));
             }
             ++uc;
             float4 ring0[kRowsPerProducer][2], ring1[kRowsPerProducer][2], ring2[kRowsPerProducer][2];

@@ -483,6 +483,23 @@ def test_grouped_f16_tensor_core_row_scales(oracle_mod, precision):
     r.check_map(oracle_mod)
 
 
+def test_grouped_f16_several_units_per_cta(oracle_mod):
+    """f16 weights with more work units than SMs (4096 routed rows over 8
+    experts x 8 output blocks of 512, the last round cut into 256-column
+    halves), so every CTA runs two or three units: the first unit's row scales
+    come from the producer warps, the later ones from the epilogue warps
+    through both shared-memory buffers.  Rows of mixed magnitude; every
+    output."""
+    m, top_k, E, n, k = 1024, 4, 8, 4000, 136
+    c = synth.matmul_id_case("f16units", "f16", m, n, k, top_k, E, route=1, seed=31)
+    rows = c.x.reshape(m, k)
+    rows[::3] *= np.float32(5e6)
+    rows[1::5] *= np.float32(3e-7)
+    r = Run(c).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+    r.check(oracle_mod)
+
+
 @pytest.mark.parametrize("count", [1, 17, 64, 65, 128, 200])
 def test_grouped_f16_tail_and_full_blocks(oracle_mod, count):
     """f16 weights: an expert list of `count` routed rows (tail units for at
