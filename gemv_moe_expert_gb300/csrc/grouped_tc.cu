@@ -35,15 +35,18 @@
 //              evict-last: each token row serves top_k experts) two k-blocks
 //              ahead of use, split into bf16 hi / lo, write the 128-byte-
 //              swizzled K-major smem layout the MMA descriptors expect.
-// Shared memory: an activation ring of 3 stages x (x_hi 16 KB + x_lo 16 KB)
+// Shared memory: an activation ring of 4 stages x (x_hi 16 KB + x_lo 16 KB)
 // and a weight ring of 3 stages x one 256x64 tile (32 KB).  The weight ring
 // runs a half k-block at a time: a weight stage is refilled as soon as the
-// MMAs of its half are done.  Both rings need depth: at the same 192 KB,
-// 3 + 3 stages run 9 % faster than 4 weight + 2 activation stages, and 2 + 4
-// no faster than 4 + 2 (measured on the MoE prefill workload).
+// MMAs of its half are done.  The activation ring's depth is what the time
+// follows (measured on the MoE prefill workload): 4 + 3 stages run 4 %
+// faster than 3 + 3, 3 + 4 are slower than 3 + 3, and at 192 KB 3 + 3 beat
+// 4 weight + 2 activation stages by 9 %.
 // Tile list: every CTA derives it from expert_counts (written by the map
 // launch before this one): tiles ordered by expert, then row block, then
-// output block.  Every mbarrier wait is bounded; see gemm_tc.cu.
+// output block, located through a tile prefix kept for every 8th expert (to
+// leave the shared memory to the rings).  Every mbarrier wait is bounded;
+// see gemm_tc.cu.
 //
 // Tail units.  An expert's last row block often holds only a few routed rows
 // (on the Zipf prefill workload 69 of 128 experts end on a block of at most
@@ -83,7 +86,7 @@ constexpr uint32_t kTailCols = 128;  // TMEM columns between the accumulators of
 constexpr int kBNH = 256;          // one accumulator / one MMA N
 constexpr int kBN = 2 * kBNH;      // tile width
 constexpr int kBK = 64;
-constexpr int kXStages = 3;         // activation stages (x_hi + x_lo of one k-block)
+constexpr int kXStages = 4;         // activation stages (x_hi + x_lo of one k-block)
 constexpr int kWStages = 3;         // weight stages (one 256-row half of a k-block)
 constexpr int kThreads = 448;
 constexpr int kRowsPerProducer = 4;  // 8 producer warps x 32 row groups x 4 = 128 rows
@@ -97,7 +100,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kRingBytes = kWBase + kWStages * kWBytes;
 constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 10;  // + row-scale barriers (f16 weights)
-constexpr uint32_t kSmemBytes = kRingBytes + (kMaxExperts + 8) * 4 + 2 * kBM * 4 + 8 * kNumBars + 16 + 1024;
+// Tile prefix kept for every kPrefixStep-th expert only (the experts between
+// are walked from their counts), so that four activation stages fit.
+constexpr int kPrefixStep = 8;
+constexpr uint32_t kPrefixBytes = (kMaxExperts / kPrefixStep + 2) * 4;  // coarse prefix + total tiles
+constexpr uint32_t kRexpBytes = 2 * kBM;                                 // int8 row-scale exponents (f16)
+constexpr uint32_t kSmemBytes = kRingBytes + kPrefixBytes + kRexpBytes + 8 * kNumBars + 16 + 1024;
+static_assert((kPrefixBytes + kRexpBytes) % 8 == 0, "mbarriers need 8-byte alignment");
+static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM: shared memory within the opt-in limit");
 
 static_assert(kTailLo % 8 == 0 && kTailRows <= kTailLo && kTailLo + kTailRows <= kBM,
               "a tail unit's hi and lo rows share the 128-row x_hi operand, in the same swizzle phase");
@@ -118,20 +128,36 @@ __device__ __forceinline__ uint32_t tail_n(int rows) {
     return kSplit ? static_cast<uint32_t>(kTailLo) + r16 : r16;
 }
 
-// expert of tile t: the largest e with prefix[e] <= t (prefix has E+1 entries)
-__device__ __forceinline__ GroupedTile decode_grouped(int t, const uint32_t *prefix, int E, int nblk,
+// row blocks x output blocks of expert e (its count read from the map's scratch)
+__device__ __forceinline__ int expert_tiles(const uint32_t *counts, int e, int m, int nblk) {
+    const int c = min(static_cast<int>(counts[e]), m);
+    return (c + kBM - 1) / kBM * nblk;
+}
+
+// Tile t: expert e, row block, output block.  coarse[j] = tiles of experts
+// below kPrefixStep * j; the largest j with coarse[j] <= t (of ceil(E / step)
+// entries) gives the expert group, whose experts are then walked.
+__device__ __forceinline__ GroupedTile decode_grouped(int t, const uint32_t *coarse, int E, int nblk,
                                                       const uint32_t *counts, int m) {
-    int lo = 0, hi = E;  // invariant prefix[lo] <= t < prefix[hi]
+    int lo = 0, hi = (E + kPrefixStep - 1) / kPrefixStep;  // coarse[lo] <= t; t < coarse[hi] if hi < count
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= static_cast<uint32_t>(t)) lo = mid; else hi = mid;
+        if (coarse[mid] <= static_cast<uint32_t>(t)) lo = mid; else hi = mid;
+    }
+    int e = lo * kPrefixStep;
+    int base = static_cast<int>(coarse[lo]);
+    const int e_end = min(E, e + kPrefixStep);
+    for (; e + 1 < e_end; ++e) {
+        const int te = expert_tiles(counts, e, m, nblk);
+        if (t < base + te) break;
+        base += te;
     }
     GroupedTile g;
-    g.e = lo;
-    const int local = t - static_cast<int>(prefix[lo]);
+    g.e = e;
+    const int local = t - base;
     g.mb = local / nblk;
     g.nb = local % nblk;
-    const int cnt = min(static_cast<int>(counts[lo]), m);
+    const int cnt = min(static_cast<int>(counts[e]), m);
     g.rows = min(kBM, cnt - g.mb * kBM);
     g.tail = g.rows <= kTailRows;
     return g;
@@ -223,8 +249,9 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     // activation stage s at s_base + s*kXStageBytes (x_hi, x_lo); weight stage
     // s at s_base + kWBase + s*kWBytes
     uint32_t *prefix = reinterpret_cast<uint32_t *>(smem + kRingBytes);
-    int *rexp_s = reinterpret_cast<int *>(prefix + kMaxExperts + 8);  // [2][kBM] row scale exponents (f16)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(rexp_s + 2 * kBM);
+    // coarse tile prefix, then the total tile count at prefix[kMaxExperts / kPrefixStep + 1]
+    int8_t *rexp_s = reinterpret_cast<int8_t *>(smem + kRingBytes + kPrefixBytes);  // [2][kBM] (f16)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes + kPrefixBytes + kRexpBytes);
     const uint32_t bar0 = smem_addr(bars);
     auto xfull_bar = [&](int s) { return bar0 + 8u * s; };
     auto xempty_bar = [&](int s) { return bar0 + 8u * (kXStages + s); };
@@ -280,7 +307,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         tmem_relinquish();
     }
 
-    // tile prefix over experts: prefix[e] = sum_{e' < e} ceil(count/128) * nblk
+    // tile prefix over experts, sum_{e' < e} ceil(count/128) * nblk, kept for
+    // e a multiple of kPrefixStep, and the total
     {
         constexpr int kPer = 3;  // 448 threads x 3 >= 1024 + 1 entries
         uint32_t v[kPer];
@@ -310,7 +338,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
             const int e = threadIdx.x * kPer + q;
-            if (e <= E) prefix[e] = run;
+            if (e == E) prefix[kMaxExperts / kPrefixStep + 1] = run;
+            else if (e < E && e % kPrefixStep == 0) prefix[e / kPrefixStep] = run;
             run += v[q];
         }
     }
@@ -318,7 +347,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = static_cast<int>(prefix[E]);
+    const int num_tiles = static_cast<int>(prefix[kMaxExperts / kPrefixStep + 1]);
     const int grid = static_cast<int>(gridDim.x);
     const int tail = num_tiles > grid ? num_tiles % grid : (2 * num_tiles <= grid ? num_tiles : 0);
     const int split_from = num_tiles - tail;
@@ -522,7 +551,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                 }
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                if (sub == 0) rexp_s[b * kBM + i] = row_scale_exp(mx);
+                if (sub == 0) rexp_s[b * kBM + i] = static_cast<int8_t>(row_scale_exp(mx));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sfull_bar(b));
@@ -541,7 +570,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         for (; u < num_units && ok;) {
             const GroupedTile g = decode_unit(u, split_from, prefix, E, nblk, p.counts, m, p.n);
             const int sb = static_cast<int>(uc & 1u);
-            const int *rexp = rexp_s + sb * kBM;
+            const int8_t *rexp = rexp_s + sb * kBM;
             if (kF16) {
                 // this unit's scales, complete from all their writers
                 const bool ready = uc == 0 ? warp_wait(s0_bar, 0u, lim, abort_flag, lane)
@@ -729,7 +758,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     for (int o = 1; o < 8; o <<= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
                     const int se = row_scale_exp(mx[q]);
                     scl[q] = pow2f(se);
-                    if (sub == 0) rexp_s[rsub + 32 * q] = se;  // buffer 0, for the epilogue
+                    if (sub == 0) rexp_s[rsub + 32 * q] = static_cast<int8_t>(se);  // buffer 0, for the epilogue
                 }
                 __syncwarp();
                 if (lane == 0) {
