@@ -450,6 +450,11 @@ FFMA_WIDE_CASES = [
     ("f32", 4, 1030, 650, 200, True, False, None, 651),     # tn, C rows padded to an odd pitch (scalar stores)
     ("f32", 4, 1030, 650, 200, True, True, None, None),     # tt
     ("f16", 2, 1664, 1536, 72, False, True, 75, None),      # f16 rows TMA cannot read (odd lda)
+    # interior-only grids with 16-byte-loadable f32 operands: the vector-load FFMA kernel
+    ("f32", 2, 1280, 1024, 208, False, False, 212, None),  # nn, A rows padded to a multiple of 4
+    ("f32", 2, 1280, 1024, 208, False, True, None, 1028),  # nt, C rows padded
+    ("f32", 2, 1280, 1024, 208, True, False, 1284, None),  # tn, A stored [k, m] with padded rows
+    ("f32", 2, 1280, 1024, 208, True, True, None, None),   # tt
 ]
 
 
