@@ -483,6 +483,23 @@ def test_grouped_f16_tensor_core_row_scales(oracle_mod, precision):
     r.check_map(oracle_mod)
 
 
+@pytest.mark.parametrize("wdtype", ["bf16", "f16"])
+def test_grouped_tc_expert_groups_with_gaps(oracle_mod, wdtype):
+    """21 experts (not a multiple of the tile prefix's 8-expert step) with
+    lists of 0 to 500 routed rows, empty experts inside and at the ends of the
+    8-expert groups: the tile order walks each group's experts from their
+    counts.  Top-1 routing; every output and the map."""
+    sizes = [0, 300, 0, 129, 64, 65, 0, 1, 200, 0, 128, 256, 0, 0, 77, 500, 3, 0, 130, 1, 0]
+    ids = np.concatenate([np.full(c_, e, dtype=np.uint32) for e, c_ in enumerate(sizes)])
+    ids = np.random.default_rng(21).permutation(ids).reshape(-1, 1)
+    m, E = ids.shape[0], len(sizes)
+    c = synth.matmul_id_case(f"groups-{wdtype}", wdtype, m, 600, 136, 1, E, route=1, ids=ids, seed=21)
+    r = Run(c).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+    r.check(oracle_mod)
+    r.check_map(oracle_mod)
+
+
 def test_grouped_f16_several_units_per_cta(oracle_mod):
     """f16 weights with more work units than SMs (4096 routed rows over 8
     experts x 8 output blocks of 512, the last round cut into 256-column
