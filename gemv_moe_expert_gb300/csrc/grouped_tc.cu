@@ -636,6 +636,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             float *orow = p.out + r * p.n;
             const float rs = kF16 ? pow2f(-rexp[i]) : 1.f;  // exact power of two
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            const uint64_t spol = policy_evict_first();
             constexpr int kChunksPerHalf = kBNH / 32;
             static_assert(kChunksPerHalf % 2 == 0, "chunks are read in pairs");
             const int nch = g.halves * kChunksPerHalf;
@@ -647,13 +648,14 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
                     for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * rs);
                 }
                 if (out_vec_ok == 2 && j0 + 32 <= p.n) {
-                    // whole 32-byte sectors per store: no partial-sector writes in L2
+                    // whole 32-byte sectors per store: no partial-sector writes in L2;
+                    // not kept in L1, evict-first in L2 (1 % faster than .cs stores)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         asm volatile(
-                            "st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + j0 + 8 * q),
+                            "st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(orow + j0 + 8 * q),
                             "r"(v[8 * q]), "r"(v[8 * q + 1]), "r"(v[8 * q + 2]), "r"(v[8 * q + 3]),
-                            "r"(v[8 * q + 4]), "r"(v[8 * q + 5]), "r"(v[8 * q + 6]), "r"(v[8 * q + 7])
+                            "r"(v[8 * q + 4]), "r"(v[8 * q + 5]), "r"(v[8 * q + 6]), "r"(v[8 * q + 7]), "l"(spol)
                             : "memory");
                 } else if (out_vec_ok && j0 + 32 <= p.n) {
                     float4 *dst = reinterpret_cast<float4 *>(orow + j0);
