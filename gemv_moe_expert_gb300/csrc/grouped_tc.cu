@@ -30,7 +30,12 @@
 //   warp 1     TMEM allocation (512 columns) and the MMA issuer:
 //              16 x tcgen05.mma (M=128, N=256, K=16) per 64-wide k-block
 //   warps 2..5 epilogue: TMEM -> registers -> f32 rows of `out`, scattered to
-//              their routed rows (each thread writes 128 contiguous bytes)
+//              their routed rows (each thread writes 128 contiguous bytes per
+//              32 columns, L1 bypassed, L2 evict-first); the next 32 TMEM
+//              columns are read while the current ones are stored, and each
+//              256-column accumulator half has its own full / empty barrier
+//              pair, so a half is drained and handed back while the MMAs of
+//              the other still run
 //   warps 6..13 activation producers: gather the 128 routed x rows (f32, L2
 //              evict-last: each token row serves top_k experts) two k-blocks
 //              ahead of use, split into bf16 hi / lo, write the 128-byte-
