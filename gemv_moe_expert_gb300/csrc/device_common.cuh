@@ -188,6 +188,16 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it in the stream still
+// runs; griddepcontrol.wait blocks until that kernel has completed and its
+// memory operations are visible (a no-op when launched without the
+// attribute), and launch_dependents lets the next such kernel start early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Bring the 128-byte line holding p into L2, marked evict-last.
 __device__ __forceinline__ void prefetch_l2_evict_last(const void *p) {
     asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));

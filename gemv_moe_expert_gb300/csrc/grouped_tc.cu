@@ -312,6 +312,11 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
         tmem_relinquish();
     }
 
+    // Launched right behind the map kernel with programmatic stream
+    // serialisation: the set-up above may overlap the map's tail; nothing
+    // global is read or written before the map grid has completed.
+    grid_dep_wait();
+
     // tile prefix over experts, sum_{e' < e} ceil(count/128) * nblk, kept for
     // e a multiple of kPrefixStep, and the total
     {
@@ -899,8 +904,19 @@ cudaError_t grouped_tc_t(const CUtensorMap &map_w, const MatmulIdParams &p, int 
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    grouped_tc_kernel<kSplit, kF16><<<num_sms, kThreads, kSmemBytes, s>>>(map_w, p, out_vec_ok);
-    return cudaGetLastError();
+    // may start while the map kernel before it finishes (it waits for it
+    // before touching global memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_tc_kernel<kSplit, kF16>, map_w, p, out_vec_ok);
 }
 }  // namespace
 

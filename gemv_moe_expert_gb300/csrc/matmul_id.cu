@@ -256,6 +256,9 @@ constexpr int kMapBatch = 16;  // ids per lane held in registers per step
 constexpr int kMapCluster = 8; // CTAs of the cluster that builds the map
 
 __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdParams p) {
+    // the grouped GEMM launched after this kernel may start its prologue now;
+    // it waits for this grid's completion before it reads the map
+    grid_dep_launch_dependents();
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
