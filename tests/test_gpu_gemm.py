@@ -468,6 +468,20 @@ def test_ffma_wide_tile_parity(oracle_mod, case):
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
 
 
+@pytest.mark.parametrize("ta,tb,bcast", [(False, True, "a"), (True, False, "b"), (False, False, "a")])
+def test_ffma_vector_tile_broadcast_and_offsets(oracle_mod, ta, tb, bcast):
+    """The vector-load FFMA tile (f32 grid of interior tiles) with a broadcast
+    operand (batch stride 0), padded leading dimensions and 16-byte aligned
+    byte offsets; every output against the oracle."""
+    batch, m, n, k = 3, 1024, 1024, 48
+    lda = (m if ta else k) + 4
+    ldb = (k if tb else n) + 8
+    g = StridedGemm("f32", batch, m, n, k, ta, tb, lda=lda, ldb=ldb, ldc=n + 4,
+                    sa=0 if bcast == "a" else None, sb=0 if bcast == "b" else None,
+                    a_off=16, b_off=48, c_off=32, std=1.0 / np.sqrt(k), seed=5 + ta + 2 * tb)
+    run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+
+
 SKINNY_SPLIT_CASES = [
     # dtype, m, n, k, lda, ldc: what the case covers (cluster split chosen by the library)
     ("f16", 5, 300, 1000, None, None),    # ragged k (15 blocks + 40), 3 tiles, a 3-way split of 16 k-blocks
