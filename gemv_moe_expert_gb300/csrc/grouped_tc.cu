@@ -45,8 +45,8 @@
 // runs a half k-block at a time: a weight stage is refilled as soon as the
 // MMAs of its half are done.  The activation ring's depth is what the time
 // follows (measured on the MoE prefill workload): 4 + 3 stages run 4 %
-// faster than 3 + 3, 3 + 4 are slower than 3 + 3, and at 192 KB 3 + 3 beat
-// 4 weight + 2 activation stages by 9 %.
+// faster than 3 + 3, 3 + 4 are slower than 3 + 3, 5 + 2 13 % slower than
+// 4 + 3, and at 192 KB 3 + 3 beat 4 weight + 2 activation stages by 9 %.
 // Tile list: every CTA derives it from expert_counts (written by the map
 // launch before this one): tiles ordered by expert, then row block, then
 // output block, located through a tile prefix kept for every 8th expert (to
