@@ -388,6 +388,11 @@ __global__ void __launch_bounds__(kMapThreads) matmul_id_map_kernel(MatmulIdPara
 // 16-wide k step reads four 16-byte shared-memory vectors per 64 FMAs.  The
 // next k step's tiles are loaded into registers while the current one is
 // multiplied (two shared-memory buffers, one barrier per step).
+// A row block of at most 64 routed rows runs as a 64 x 256 tile instead
+// (threads 8 x 32, rows {4 ty .., 32 + 4 ty ..}, columns {4 tx .., 128 +
+// 4 tx ..}): the same 64 FMAs per four 16-byte shared-memory reads per
+// thread, where half of a 128 x 128 tile would idle.  The CTA of the even
+// 128-column index computes both 128-column tiles; the odd one returns.
 
 constexpr int kGM = 128;
 constexpr int kGN = 128;
@@ -395,12 +400,136 @@ constexpr int kGK = 16;
 constexpr int kGThreads = 256;
 constexpr int kGPitch = kGM + 4;  // keeps 16-byte alignment of each k row
 
+constexpr int kG64M = 64;
+constexpr int kG64N = 256;
+constexpr int kG64PitchA = kG64M + 4;
+constexpr int kG64PitchB = kG64N + 4;
+
+// the 64 x 256 tile of a row block of at most 64 routed rows (see above)
+template <typename TW>
+__device__ __forceinline__ void grouped_simt64(const MatmulIdParams &p, int vec_ok, int out_vec_ok, int64_t e,
+                                               int64_t cnt, int64_t i0, int64_t n0, float *smem_f,
+                                               const uint32_t *s_rows) {
+    constexpr int kV = 16 / static_cast<int>(sizeof(TW));
+    float (*As)[kGK][kG64PitchA] = reinterpret_cast<float (*)[kGK][kG64PitchA]>(smem_f);
+    float (*Bs)[kGK][kG64PitchB] =
+        reinterpret_cast<float (*)[kGK][kG64PitchB]>(smem_f + 2 * kGK * kG64PitchA);
+    const int tid = threadIdx.x;
+    const int tx = tid & 31;
+    const int ty = tid >> 5;
+    const TW *W = static_cast<const TW *>(p.w) + e * p.expert_stride_elems;
+    // x: row tid / 4, k 4 (tid % 4); weights: kV k of column (tid / (16 / kV)) + 64 h (f32) or 128 h (16-bit)
+    const int akc = (tid & 3) * 4;
+    const uint32_t rr = s_rows[tid >> 2];
+    const float *arow = rr != 0xffffffffu ? x_row(p, rr) : nullptr;
+    constexpr int kBPer = kG64N * kGK / kV / kGThreads;  // weight vectors per thread: 4 (f32) or 2
+    constexpr int kColStep = kG64N / kBPer;
+    const int bcol0 = kV == 4 ? (tid >> 2) : (tid >> 1);
+    const int bkc = kV == 4 ? (tid & 3) * 4 : (tid & 1) * 8;
+
+    auto load = [&](int64_t k0, float4 &ra, float (&rb)[kBPer * kV]) {
+        const int64_t kx = k0 + akc;
+        if (arow == nullptr) {
+            ra = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (vec_ok && kx + 4 <= p.k) {
+            ra = *reinterpret_cast<const float4 *>(arow + kx);
+        } else {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = kx + j < p.k ? arow[kx + j] : 0.f;
+            ra = make_float4(v[0], v[1], v[2], v[3]);
+        }
+#pragma unroll
+        for (int h = 0; h < kBPer; ++h) {
+            const int64_t col = n0 + bcol0 + kColStep * h;
+            const int64_t bx = k0 + bkc;
+            float *dst = rb + h * kV;
+            if (col >= p.n) {
+#pragma unroll
+                for (int j = 0; j < kV; ++j) dst[j] = 0.f;
+            } else if (vec_ok && bx + kV <= p.k) {
+                unpack16<TW>(ld_stream16(W + col * p.k + bx), dst);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kV; ++j) dst[j] = bx + j < p.k ? Elem<TW>::to_f(W[col * p.k + bx + j]) : 0.f;
+            }
+        }
+    };
+    auto store = [&](int buf, const float4 &ra, const float (&rb)[kBPer * kV]) {
+        const int r = tid >> 2;
+        As[buf][akc + 0][r] = ra.x;
+        As[buf][akc + 1][r] = ra.y;
+        As[buf][akc + 2][r] = ra.z;
+        As[buf][akc + 3][r] = ra.w;
+#pragma unroll
+        for (int h = 0; h < kBPer; ++h) {
+            const int c = bcol0 + kColStep * h;
+#pragma unroll
+            for (int j = 0; j < kV; ++j) Bs[buf][bkc + j][c] = rb[h * kV + j];
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+    float4 ra;
+    float rb[kBPer * kV];
+    load(0, ra, rb);
+    store(0, ra, rb);
+    __syncthreads();
+    int cur = 0;
+    for (int64_t k0 = 0; k0 < p.k; k0 += kGK) {
+        const bool more = k0 + kGK < p.k;
+        if (more) load(k0 + kGK, ra, rb);
+#pragma unroll
+        for (int kk = 0; kk < kGK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][32 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][128 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+        }
+        if (more) store(cur ^ 1, ra, rb);
+        __syncthreads();
+        cur ^= 1;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const uint32_t orr = s_rows[(r < 4 ? 0 : 32) + 4 * ty + (r & 3)];
+        if (orr == 0xffffffffu) continue;
+        float *orow = p.out + static_cast<int64_t>(orr) * p.n;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t c0 = n0 + 128 * h + 4 * tx;
+            if (out_vec_ok && c0 + 4 <= p.n) {
+                *reinterpret_cast<float4 *>(orow + c0) =
+                    make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2], acc[r][4 * h + 3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c0 + c < p.n) orow[c0 + c] = acc[r][4 * h + c];
+            }
+        }
+    }
+}
+
 template <typename TW>
 __global__ void __launch_bounds__(kGThreads, 2) matmul_id_grouped_simt_kernel(MatmulIdParams p, int vec_ok,
                                                                                int out_vec_ok) {
     constexpr int kV = 16 / static_cast<int>(sizeof(TW));  // weight elements per 16-byte vector
-    __shared__ __align__(16) float As[2][kGK][kGPitch];
-    __shared__ __align__(16) float Bs[2][kGK][kGPitch];
+    // the 128 x 128 tile's two buffers, or the 64 x 256 tile's
+    constexpr int kSmemF128 = 2 * 2 * kGK * kGPitch;
+    constexpr int kSmemF64 = 2 * kGK * (kG64PitchA + kG64PitchB);
+    __shared__ __align__(16) float smem_f[kSmemF128 > kSmemF64 ? kSmemF128 : kSmemF64];
+    float (*As)[kGK][kGPitch] = reinterpret_cast<float (*)[kGK][kGPitch]>(smem_f);
+    float (*Bs)[kGK][kGPitch] = reinterpret_cast<float (*)[kGK][kGPitch]>(smem_f + 2 * kGK * kGPitch);
     __shared__ uint32_t s_rows[kGM];
     const int tid = threadIdx.x;
     const int tx = tid & 15;
@@ -413,6 +542,13 @@ __global__ void __launch_bounds__(kGThreads, 2) matmul_id_grouped_simt_kernel(Ma
     const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kGN;
     if (tid < kGM) s_rows[tid] = i0 + tid < cnt ? p.routed_rows[e * p.m + i0 + tid] : 0xffffffffu;
     __syncthreads();
+    if (cnt - i0 <= kG64M) {
+        // at most 64 routed rows: the 64 x 256 tile, computed by the CTA of the
+        // even 128-column index
+        if (blockIdx.y & 1) return;
+        grouped_simt64<TW>(p, vec_ok, out_vec_ok, e, cnt, i0, n0, smem_f, s_rows);
+        return;
+    }
     const TW *W = static_cast<const TW *>(p.w) + e * p.expert_stride_elems;
 
     // this thread's global sources
@@ -481,8 +617,7 @@ __global__ void __launch_bounds__(kGThreads, 2) matmul_id_grouped_simt_kernel(Ma
 #pragma unroll
         for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
 
-    // RN = 8: all 128 rows; RN = 4: the block holds at most 64 routed rows, so
-    // the upper 64 (all padding) are neither loaded nor multiplied
+    // all 128 rows (blocks of at most 64 took the 64 x 256 tile above)
     auto mainloop = [&](auto rows_c) {
         constexpr int RN = decltype(rows_c)::value;
         float4 ra[2];
@@ -512,10 +647,7 @@ __global__ void __launch_bounds__(kGThreads, 2) matmul_id_grouped_simt_kernel(Ma
             cur ^= 1;
         }
     };
-    if (cnt - i0 <= 64)
-        mainloop(std::integral_constant<int, 4>{});
-    else
-        mainloop(std::integral_constant<int, 8>{});
+    mainloop(std::integral_constant<int, 8>{});
 
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
