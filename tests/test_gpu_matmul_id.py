@@ -459,6 +459,25 @@ def test_grouped_ffma_row_block_sizes(oracle_mod, wdtype):
     r.check_map(oracle_mod)
 
 
+@pytest.mark.parametrize("wdtype", ["f32"])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_grouped_ffma_small_blocks_odd_column_tiles(oracle_mod, wdtype, layout):
+    """The FFMA grouped kernel's 64 x 256 tile for row blocks of at most 64
+    routed rows with an odd number of 128-column tiles (n = 300: the CTAs of
+    column tiles 0 and 2 compute 256 columns each, the last one ragged) next to
+    128 x 128 tiles of larger blocks; ragged k; every output and the map."""
+    sizes = [40, 64, 65, 130, 1, 0, 200]
+    ids = np.concatenate([np.full(c_, e, dtype=np.uint32) for e, c_ in enumerate(sizes)])
+    ids = np.random.default_rng(7).permutation(ids).reshape(-1, 1)
+    m, E = ids.shape[0], len(sizes)
+    c = synth.matmul_id_case(f"ffma-small-{layout}", wdtype, m, 300, 70, 1, E, route=1, input_layout=layout,
+                             ids=ids, seed=17)
+    r = Run(c).call()
+    assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_simt"
+    r.check(oracle_mod)
+    r.check_map(oracle_mod)
+
+
 @pytest.mark.parametrize("precision", [0, 1])
 def test_grouped_f16_tensor_core_row_scales(oracle_mod, precision):
     """GroupedPrefill with f16 weights on the grouped tensor-core kernel: each
