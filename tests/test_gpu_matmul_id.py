@@ -13,7 +13,7 @@ torch = pytest.importorskip("torch")
 
 from gemv_moe_expert_gb300 import binding as gb  # noqa: E402
 from gemv_moe_expert_gb300 import synth  # noqa: E402
-from tests.gpu_util import DevBuf, assert_close  # noqa: E402
+from tests.gpu_util import GUARD, DevBuf, assert_close  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -551,6 +551,47 @@ def test_grouped_f16_tail_and_full_blocks(oracle_mod, count):
     rows[1::6] *= np.float32(2e-9)
     r = Run(c).call()
     assert gb.gbmm_test_last_kernel() == "gbmm_matmul_id_grouped_tc"
+    r.check(oracle_mod)
+
+
+@pytest.mark.parametrize("wdtype", ["bf16", "f16"])
+def test_grouped_call_replays_from_a_cuda_graph(oracle_mod, wdtype):
+    """GroupedPrefill captured into a CUDA graph (its map launch, then the
+    grouped tensor-core kernel launched with programmatic stream serialisation
+    behind it) and replayed twice, with new activations and new expert ids
+    copied into the same buffers before the second replay: both replays match
+    the oracle, map included."""
+    c = synth.matmul_id_case(f"graph-{wdtype}", wdtype, 300, 520, 264, 4, 12, route=1, seed=41)
+    r = Run(c)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def launch():
+        st, _ = gb.gbmm_matmul_id(r.params, c.wdtype, r.w.ptr, c.w.nbytes, r.x.ptr, c.x.nbytes, r.ids.ptr,
+                                  c.ids.nbytes, r.out.ptr, r.cap.required_output_bytes, r.scratch)
+        assert st == gb.GBMM_OK, gb.gbmm_last_error()
+
+    with torch.cuda.stream(s):
+        launch()  # outside the capture: kernel attributes set, modules loaded
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        launch()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+    r.check(oracle_mod)
+    # new inputs in the same buffers, second replay
+    c2 = synth.matmul_id_case(f"graph2-{wdtype}", wdtype, 300, 520, 264, 4, 12, route=1, seed=42)
+    c2.w = c.w  # same weights, new activations and ids
+    for buf, host in ((r.x, c2.x), (r.ids, c2.ids)):
+        raw = np.ascontiguousarray(host).reshape(-1).view(np.uint8)
+        buf.t[GUARD:GUARD + raw.size].copy_(torch.from_numpy(raw.copy()))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+    r.case = c2
     r.check(oracle_mod)
 
 
