@@ -17,7 +17,7 @@ torch = pytest.importorskip("torch")
 
 from gemv_moe_expert_gb300 import binding as gb  # noqa: E402
 from gemv_moe_expert_gb300 import synth  # noqa: E402
-from tests.gpu_util import (DevBuf, StridedGemm, NP_DT, assert_close, to_f64)  # noqa: E402
+from tests.gpu_util import (GUARD, DevBuf, StridedGemm, NP_DT, assert_close, to_f64)  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -480,6 +480,41 @@ def test_ffma_vector_tile_broadcast_and_offsets(oracle_mod, ta, tb, bcast):
                     sa=0 if bcast == "a" else None, sb=0 if bcast == "b" else None,
                     a_off=16, b_off=48, c_off=32, std=1.0 / np.sqrt(k), seed=5 + ta + 2 * tb)
     run_case(oracle_mod, g, expect_kernel="gbmm_gemm_simt")
+
+
+def test_gemm_and_gemv_replay_from_a_cuda_graph(oracle_mod):
+    """A tensor-core GEMM, the m == 1 stream GEMV and the skinny tensor-core
+    GEMV captured into one CUDA graph and replayed: every output of each
+    against the oracle (stream order inside the graph is the library's only
+    synchronisation)."""
+    cases = [(StridedGemm("bf16", 2, 512, 640, 520, False, True, std=1.0 / np.sqrt(520), seed=3), "gbmm_gemm_tc"),
+             (StridedGemm("f16", 1, 1, 2048, 1024, False, True, std=1.0 / 32, seed=4), "gbmm_gemv_stream"),
+             (StridedGemm("f16", 1, 6, 1300, 1024, False, True, std=1.0 / 32, seed=5), "gbmm_gemv_tc")]
+    bufs = [g.device() for g, _ in cases]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def launch_all():
+        for (g, name), (a, b, c) in zip(cases, bufs):
+            st = gb.gbmm_gemm(*g.args(a, b, c))
+            assert st == gb.GBMM_OK, gb.gbmm_last_error()
+            assert gb.gbmm_test_last_kernel() == name
+
+    with torch.cuda.stream(s):
+        launch_all()  # outside the capture: kernel attributes set, modules loaded
+    torch.cuda.synchronize()
+    for g, (a, b, c) in zip((g for g, _ in cases), bufs):
+        c.t[GUARD:GUARD + c.nbytes].fill_(0x7F)  # garbage the graph must overwrite
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        launch_all()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+    for (g, _), (a, b, c) in zip(cases, bufs):
+        ref, ref_abs = g.oracle(oracle_mod)
+        assert_close(g.gather_c(c), ref, ref_abs, g.dtype, g.dtype, "graph replay")
 
 
 SKINNY_SPLIT_CASES = [
