@@ -129,3 +129,43 @@ def test_static_scratch_refuses_what_it_cannot_hold():
     finally:
         gb.gbmm_test_inject_kernel_failure(None)
     torch.cuda.synchronize()
+
+
+def test_static_scratch_call_replays_from_a_cuda_graph(oracle_mod):
+    """The use the entry point exists for: after one call on the device (which
+    loads the array), the call is captured into a CUDA graph and replayed with
+    new ids copied into the same buffer; each replay matches the oracle."""
+    m, n, k, top_k, E = 200, 264, 256, 4, 12
+    case = synth.matmul_id_case("noalloc-graph", "bf16", m, n, k, top_k, E, route=1, seed=31)
+    p = gb.make_params(m, n, k, top_k, E, case.expert_stride_bytes, route=gb.ROUTE_GROUPED_PREFILL)
+    st, cap = gb.gbmm_matmul_id_capability("bf16", p)
+    assert st == gb.GBMM_OK
+    w, x = _up(case.w), _up(case.x)
+    ids = _up(case.ids)
+    out = torch.empty(cap.required_output_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def launch():
+        st, _ = gb.gbmm_matmul_id_static_scratch(p, "bf16", w, case.w.nbytes, x, case.x.nbytes, ids,
+                                                 case.ids.nbytes, out, cap.required_output_bytes)
+        assert st == gb.GBMM_OK, gb.gbmm_last_error()
+
+    with torch.cuda.stream(s):
+        launch()  # before any capture: loads the array and sets kernel attributes
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        launch()
+    for seed in (31, 32):
+        ids_np = synth.distinct_ids(m, top_k, E, seed=seed)
+        ids.copy_(_up(ids_np))
+        out.fill_(0xAB)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gb.gbmm_device_error()[0] == gb.GBMM_OK
+        got = out.cpu().numpy().view(np.float32).astype(np.float64)
+        ref, ref_abs = oracle_mod.matmul_id("bf16", m, n, k, top_k, E, case.expert_stride_bytes, 0,
+                                            case.w, case.x, ids_np)
+        assert_close(got, ref.reshape(-1), ref_abs.reshape(-1), "bf16", "f32", f"graph replay, ids seed {seed}")
