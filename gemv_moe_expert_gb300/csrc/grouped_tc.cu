@@ -598,7 +598,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap map_w, const MatmulIdParam
             // the next one (its buffer is this unit's), while the next runs
             auto advance = [&]() {
                 const int u2 = u1 < num_units ? next_unit(u1) : num_units;
-                if (kF16 && u2 < num_units && !(ok = row_scales(u2, uc + 2)) && lane == 0) {
+                if (kF16 && ok && u2 < num_units && !(ok = row_scales(u2, uc + 2)) && lane == 0) {
                     *abort_flag = 1;
                     report_device_error(p.err, kKidGroupedTc);
                 }
