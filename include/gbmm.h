@@ -17,6 +17,14 @@
  *     nothing.  gbmm_last_error() then describes the failure.
  *   - Thread safety: calls may be made from several host threads; the error
  *     string is per thread.
+ *   - CUDA graphs: every call can be captured into a graph once the same
+ *     call has run on the device outside the capture (the first call on a
+ *     device sets kernel attributes, allocates the device error word and
+ *     loads modules, none of which a capture allows); replays read whatever
+ *     the captured buffers hold.  GroupedPrefill's grouped kernel is launched
+ *     with programmatic stream serialisation behind the map kernel and waits
+ *     for it before touching global memory, which a capture keeps.  Not with
+ *     GBMM_DEBUG_SYNC=1 (it synchronises the stream).
  *   - Debugging: with the environment variable GBMM_DEBUG_SYNC=1 (read once
  *     per process) every launch is followed by a stream synchronisation, so a
  *     kernel that fails on the device is reported by the call that launched
