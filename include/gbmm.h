@@ -19,8 +19,8 @@
  *     string is per thread.
  *   - CUDA graphs: every call can be captured into a graph once the same
  *     call has run on the device outside the capture (the first call on a
- *     device sets kernel attributes, allocates the device error word and
- *     loads modules, none of which a capture allows); replays read whatever
+ *     device sets kernel attributes, looks up the device error word and loads
+ *     modules, which a capture does not allow); replays read whatever
  *     the captured buffers hold.  GroupedPrefill's grouped kernel is launched
  *     with programmatic stream serialisation behind the map kernel and waits
  *     for it before touching global memory, which a capture keeps.  Not with
